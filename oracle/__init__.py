@@ -1,0 +1,21 @@
+"""fp64 CPU oracle of the NEO-unify generation-pass hot path.
+
+TEST INFRASTRUCTURE: imported only by tests/, by the smoke check in
+__graft_entry__ and by the CPU-baseline leg of bench.py. The CUDA library and
+its Python binding never import it; the two share no code.
+"""
+
+from .neo_oracle import (  # noqa: F401
+    HEAD_DIM,
+    MASK_BLOCK_CAUSAL,
+    MASK_FULL,
+    flow_euler_step,
+    flow_interpolant,
+    flow_target_velocity,
+    gen_attention,
+    positions,
+    qknorm_halves,
+    qknorm_rope3,
+    rope3,
+    rope_slices,
+)

@@ -1,0 +1,31 @@
+// Status strings, the device error word and the wait limit of libneo.
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "neo.h"
+#include "neo_internal.h"
+
+extern "C" const char* neo_status_string(neo_status s) {
+    switch (s) {
+        case NEO_OK: return "NEO_OK";
+        case NEO_ERR_INVALID_ARG: return "NEO_ERR_INVALID_ARG: an argument failed the host-side checks";
+        case NEO_ERR_UNSUPPORTED: return "NEO_ERR_UNSUPPORTED: valid arguments that this build does not implement";
+        case NEO_ERR_CUDA: return "NEO_ERR_CUDA: a CUDA call or kernel launch failed";
+        case NEO_ERR_TIMEOUT: return "NEO_ERR_TIMEOUT: a pipeline wait inside a kernel ran out of time";
+        case NEO_ERR_DEVICE: return "NEO_ERR_DEVICE: a kernel rejected its device-side inputs";
+    }
+    return "unknown neo_status";
+}
+
+extern "C" neo_status neo_get_device_error(cudaStream_t stream, uint32_t* word) {
+    return neo::attention_error_read_clear(stream, word);
+}
+
+extern "C" neo_status neo_set_wait_timeout_ns(uint64_t ns) {
+    if (ns == 0) return NEO_ERR_INVALID_ARG;
+    return neo::attention_set_timeout(ns);
+}
+
+extern "C" int neo_version(void) { return 100; }

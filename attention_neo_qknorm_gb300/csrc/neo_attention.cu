@@ -1,0 +1,521 @@
+// Generation-pass attention of NEO-unify on tcgen05 tensor cores.
+//
+// What it computes ("SenseNova-U1.5 (NEO-unify) architecture", sections
+// "Mixture of Transformers" items 1-2 and "GQA fusion does not apply"): every
+// noisy image token's query attends, without a mask, over the frozen prefix
+// keys/values of its own sequence followed by the image tokens' own
+// keys/values; query head h reads KV head h / (Hq/Hkv).
+//
+// Kernel shape (one CTA per 128-row query tile; D = 128):
+//   * A query tile packs the G = Hq/Hkv heads of one KV group for 128/G
+//     consecutive tokens (row r = token * G + head-in-group), so each K/V tile
+//     brought into shared memory serves the whole GQA group.
+//   * Warp 0 (one lane) streams Q once and K/V tiles of 128 keys through a
+//     two-stage TMA ring (128-byte swizzle): first the ceil(L_b/128) tiles of
+//     the packed prefix, then the image tiles. Keys past a segment's end are
+//     masked, so ragged prefixes need no padding.
+//   * Warp 1 (one lane) issues tcgen05.mma: S = Q K^T (A, B K-major in smem,
+//     fp32 accumulator in TMEM, double-buffered so S_{j+1} overlaps the
+//     softmax of tile j) and O += P V (P bf16 read from TMEM, V MN-major in
+//     smem, O accumulated in TMEM).
+//   * Warps 4..7 (one thread per query row = TMEM lane) run the online
+//     softmax in fp32 with exp2 on the SFU, store P to TMEM, rescale O only
+//     when the running maximum grew by more than 2^8 (the final division uses
+//     the same stale maximum, so the result is unchanged), and finally write
+//     O / l as bf16 through shared memory and a TMA store.
+// TMEM: S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,512).
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "neo.h"
+#include "neo_internal.h"
+#include "sm103_ptx.cuh"
+
+using namespace sm103;
+
+namespace {
+
+__device__ unsigned int g_dev_error = 0;
+__device__ unsigned long long g_wait_limit_ns = 1000000000ull;
+
+constexpr int kThreads = 256;
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kStages = 2;
+constexpr uint32_t kHalfTile = 128u * 64u * 2u;   // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr uint32_t kTile = 2u * kHalfTile;         // 128 rows x 128 bf16
+
+constexpr uint32_t kSmQ = 0;
+constexpr uint32_t kSmK = kSmQ + kTile;
+constexpr uint32_t kSmV = kSmK + kStages * kTile;
+constexpr uint32_t kSmBar = kSmV + kStages * kTile;
+
+enum : int {
+    BAR_Q_FULL = 0,
+    BAR_K_FULL = 1,
+    BAR_K_EMPTY = BAR_K_FULL + kStages,
+    BAR_V_FULL = BAR_K_EMPTY + kStages,
+    BAR_V_EMPTY = BAR_V_FULL + kStages,
+    BAR_S_FULL = BAR_V_EMPTY + kStages,
+    BAR_S_FREE = BAR_S_FULL + 2,
+    BAR_P_FULL = BAR_S_FREE + 2,
+    BAR_PV_DONE = BAR_P_FULL + 2,
+    BAR_DRAIN = BAR_PV_DONE + 2,
+    NUM_BARS = BAR_DRAIN + 1
+};
+
+constexpr uint32_t kSmTmemSlot = kSmBar + NUM_BARS * 8;
+constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
+constexpr uint32_t kSmEpiSkip = kSmAbort + 4;   // written only by the softmax warps
+constexpr uint32_t kSmUsed = kSmEpiSkip + 4;
+constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
+
+constexpr uint32_t kTmS0 = 0, kTmP0 = 256, kTmO = 384, kTmCols = 512;
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);   // Q, K both K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, 128, 0, 1);      // V is MN-major
+
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+struct AttnParams {
+    const int32_t* cu_prefix;
+    float* lse;
+    int64_t total_prefix;
+    int B, N, Hq, Hkv, G, tok_per_tile, max_prefix;
+    float scale_log2;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, int i) { return sbase + kSmBar + 8u * i; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                     const __grid_constant__ CUtensorMap tm_kimg,
+                     const __grid_constant__ CUtensorMap tm_vimg,
+                     const __grid_constant__ CUtensorMap tm_kpre,
+                     const __grid_constant__ CUtensorMap tm_vpre, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+
+    // Prefix segment of this sequence; an inconsistent cu_prefix skips the CTA.
+    const int lo = p.cu_prefix[b];
+    const int hi = p.cu_prefix[b + 1];
+    const int L = hi - lo;
+    if (lo < 0 || L < 0 || (int64_t)hi > p.total_prefix || L > p.max_prefix) {
+        if (threadIdx.x == 0) atomicOr(&g_dev_error, NEO_DEVERR_BAD_PREFIX);
+        return;
+    }
+    const int n_pre = (L + kBlockN - 1) / kBlockN;
+    const int n_img = (p.N + kBlockN - 1) / kBlockN;
+    const int n_tiles = n_pre + n_img;
+    const int n0 = qt * p.tok_per_tile;
+
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmAbort);
+    const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
+
+    volatile int* epi_skip = reinterpret_cast<volatile int*>(smem + kSmEpiSkip);
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        *epi_skip = 0;
+        for (int i = 0; i < NUM_BARS; ++i) {
+            uint32_t count = 1;
+            if (i == BAR_S_FREE || i == BAR_S_FREE + 1 || i == BAR_P_FULL || i == BAR_P_FULL + 1) count = 128;
+            mbar_init(bar_addr(sb, i), count);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + kSmTmemSlot, kTmCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t sQ = sb + kSmQ;
+            mbar_arrive_expect_tx(bar_addr(sb, BAR_Q_FULL), kTile);
+            tma_load_4d(sQ, &tm_q, bar_addr(sb, BAR_Q_FULL), 0, kvh * p.G, n0, b);
+            tma_load_4d(sQ + kHalfTile, &tm_q, bar_addr(sb, BAR_Q_FULL), 64, kvh * p.G, n0, b);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % kStages;
+                const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+                const uint32_t sK = sb + kSmK + st * kTile;
+                const uint32_t sV = sb + kSmV + st * kTile;
+                if (!wait(bar_addr(sb, BAR_K_EMPTY + st), ph ^ 1u)) break;
+                const uint32_t kf = bar_addr(sb, BAR_K_FULL + st);
+                mbar_arrive_expect_tx(kf, kTile);
+                if (j < n_pre) {
+                    const int row = lo + j * kBlockN;
+                    tma_load_3d(sK, &tm_kpre, kf, 0, kvh, row);
+                    tma_load_3d(sK + kHalfTile, &tm_kpre, kf, 64, kvh, row);
+                } else {
+                    const int row = (j - n_pre) * kBlockN;
+                    tma_load_4d(sK, &tm_kimg, kf, 0, kvh, row, b);
+                    tma_load_4d(sK + kHalfTile, &tm_kimg, kf, 64, kvh, row, b);
+                }
+                k_issued = j + 1;
+                if (!wait(bar_addr(sb, BAR_V_EMPTY + st), ph ^ 1u)) break;
+                const uint32_t vf = bar_addr(sb, BAR_V_FULL + st);
+                mbar_arrive_expect_tx(vf, kTile);
+                if (j < n_pre) {
+                    const int row = lo + j * kBlockN;
+                    tma_load_3d(sV, &tm_vpre, vf, 0, kvh, row);
+                    tma_load_3d(sV + kHalfTile, &tm_vpre, vf, 64, kvh, row);
+                } else {
+                    const int row = (j - n_pre) * kBlockN;
+                    tma_load_4d(sV, &tm_vimg, vf, 0, kvh, row, b);
+                    tma_load_4d(sV + kHalfTile, &tm_vimg, vf, 64, kvh, row, b);
+                }
+                v_issued = j + 1;
+            }
+            if (*abort_flag) {
+                // Let copies already in flight land before the CTA's shared memory goes away.
+                wait(bar_addr(sb, BAR_Q_FULL), 0, false);
+                for (int j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
+                    wait(bar_addr(sb, BAR_K_FULL + j % kStages), (uint32_t)(j / kStages) & 1u, false);
+                for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
+                    wait(bar_addr(sb, BAR_V_FULL + j % kStages), (uint32_t)(j / kStages) & 1u, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sQ = sb + kSmQ;
+            bool ok = wait(bar_addr(sb, BAR_Q_FULL), 0);
+            tc_fence_after();
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % kStages;
+                if (!wait(bar_addr(sb, BAR_K_FULL + st), (uint32_t)(j / kStages) & 1u)) return false;
+                if (!wait(bar_addr(sb, BAR_S_FREE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u)) return false;
+                tc_fence_after();
+                const uint32_t sK = sb + kSmK + st * kTile;
+                const uint32_t d = tmem + kTmS0 + (uint32_t)(j & 1) * 128u;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
+                           kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_addr(sb, BAR_S_FULL + (j & 1)));
+                mma_commit(bar_addr(sb, BAR_K_EMPTY + st));
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                const int st = j % kStages;
+                if (!wait(bar_addr(sb, BAR_P_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u)) return false;
+                if (!wait(bar_addr(sb, BAR_V_FULL + st), (uint32_t)(j / kStages) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t sV = sb + kSmV + st * kTile;
+                const uint32_t pcol = tmem + kTmP0 + (uint32_t)(j & 1) * 64u;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    // 16 keys per step: rows 16*kk.. of V (2048 bytes); the two
+                    // 64-wide halves of the head dim are 16 KB apart.
+                    mma_ts(tmem + kTmO, pcol + (uint32_t)kk * 8u,
+                           smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_addr(sb, BAR_PV_DONE + (j & 1)));
+                mma_commit(bar_addr(sb, BAR_V_EMPTY + st));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles && !issue_s(j + 1)) break;
+                if (!issue_pv(j)) break;
+            }
+            // Drain: every MMA issued above completes before TMEM is released.
+            mma_commit(bar_addr(sb, BAR_DRAIN));
+            wait(bar_addr(sb, BAR_DRAIN), 0, false);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        float m_used = -INFINITY;
+        float l_sum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+            {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(lane_base + kTmS0 + (uint32_t)(j & 1) * 128u + c * 32u, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(sb, BAR_S_FREE + (j & 1)));
+
+            const int valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                s[c] = c < valid ? s[c] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            const float m_new = fmaxf(m_used, mx);
+            const bool need = m_new > m_used + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                if (need) m_used = m_new;
+                l_sum *= alpha;
+                if (j > 0) {
+                    ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + ((j - 1) & 1)),
+                                                      (uint32_t)((j - 1) >> 1) & 1u));
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint32_t r[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(lane_base + kTmO + c * 32u, r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(lane_base + kTmO + c * 32u, r);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            float rs = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ex2(s[2 * c] - m_used);
+                const float p1 = ex2(s[2 * c + 1] - m_used);
+                rs += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l_sum += rs;
+            if (j >= 2) {
+                // P buffer j&1 was last read by PV_{j-2}.
+                ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            {
+                const uint32_t pcol = lane_base + kTmP0 + (uint32_t)(j & 1) * 64u;
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = pk[i];
+                tmem_st32(pcol, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = pk[32 + i];
+                tmem_st32(pcol + 32u, r);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(sb, BAR_P_FULL + (j & 1)));
+        }
+
+        // Only these four warps write epi_skip, and only before this barrier,
+        // so after it every warp of the group takes the same branch.
+        if (ok) {
+            const int jl = n_tiles - 1;
+            ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (jl & 1)), (uint32_t)(jl >> 1) & 1u));
+        }
+        if (!ok) *epi_skip = 1;
+        named_barrier_sync(1, 128);
+        if (!*epi_skip) {
+            {
+                tc_fence_after();
+                const float inv_l = 1.0f / l_sum;
+                uint8_t* stage = smem + kSmQ;    // Q is no longer read once the last S is done
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + kTmO + c * 32u, r);
+                    const int half = c >> 1;
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(r[qd * 8 + 0]) * inv_l, __uint_as_float(r[qd * 8 + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(r[qd * 8 + 2]) * inv_l, __uint_as_float(r[qd * 8 + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(r[qd * 8 + 4]) * inv_l, __uint_as_float(r[qd * 8 + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(r[qd * 8 + 6]) * inv_l, __uint_as_float(r[qd * 8 + 7]) * inv_l);
+                        const int chunk = (c & 1) * 4 + qd;
+                        const uint32_t off = (uint32_t)half * kHalfTile + (uint32_t)row * 128u +
+                                             (uint32_t)((chunk ^ (row & 7)) << 4);
+                        *reinterpret_cast<uint4*>(stage + off) = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                named_barrier_sync(1, 128);
+                if (row == 0) {
+                    tma_store_4d(&tm_o, sb + kSmQ, 0, kvh * p.G, n0, b);
+                    tma_store_4d(&tm_o, sb + kSmQ + kHalfTile, 64, kvh * p.G, n0, b);
+                    tma_store_commit_and_wait_read();
+                }
+                const int n = n0 + row / p.G;
+                if (p.lse != nullptr && n < p.N) {
+                    const int h = kvh * p.G + row % p.G;
+                    p.lse[((int64_t)b * p.Hq + h) * p.N + n] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmCols);
+    }
+}
+
+// --------------------------------------------------------------------- host
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims[0] is the contiguous head dim.
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+              const uint32_t* box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[5], s[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace neo {
+
+neo_status attention_error_read_clear(cudaStream_t stream, uint32_t* word) {
+    unsigned int h = 0, zero = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NEO_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&h, g_dev_error, sizeof(h)) != cudaSuccess) return NEO_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return NEO_ERR_CUDA;
+    if (word) *word = h;
+    if (h & NEO_DEVERR_TIMEOUT) return NEO_ERR_TIMEOUT;
+    return h ? NEO_ERR_DEVICE : NEO_OK;
+}
+
+neo_status attention_set_timeout(uint64_t ns) {
+    unsigned long long v = ns;
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? NEO_OK : NEO_ERR_CUDA;
+}
+
+}  // namespace neo
+
+extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix, const void* v_prefix,
+                                        const void* k_img, const void* v_img, neo_dtype dtype,
+                                        const int32_t* cu_prefix, int64_t total_prefix, int32_t max_prefix,
+                                        int B, int N, int Hq, int Hkv, int D, neo_mask mask_mode,
+                                        const int32_t* t_prefix, const int32_t* t_img, float scale, void* out,
+                                        float* lse, cudaStream_t stream) {
+    (void)t_prefix;
+    (void)t_img;
+    if (D != 128 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return NEO_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (kBlockM % G != 0) return NEO_ERR_UNSUPPORTED;
+    if (total_prefix < 0 || max_prefix < 0 || total_prefix > 0x7fffffffLL) return NEO_ERR_INVALID_ARG;
+    if (!q_img || !k_img || !v_img || !out || !cu_prefix) return NEO_ERR_INVALID_ARG;
+    if (total_prefix > 0 && (!k_prefix || !v_prefix)) return NEO_ERR_INVALID_ARG;
+    if (!neo::aligned16(q_img) || !neo::aligned16(k_img) || !neo::aligned16(v_img) || !neo::aligned16(out) ||
+        (total_prefix > 0 && (!neo::aligned16(k_prefix) || !neo::aligned16(v_prefix))))
+        return NEO_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return NEO_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || scale < 0.f) return NEO_ERR_INVALID_ARG;
+    if (mask_mode != NEO_MASK_FULL && mask_mode != NEO_MASK_BLOCK_CAUSAL) return NEO_ERR_INVALID_ARG;
+    if (mask_mode == NEO_MASK_BLOCK_CAUSAL) return NEO_ERR_UNSUPPORTED;
+    if (dtype != NEO_BF16) return NEO_ERR_UNSUPPORTED;
+    if (B > 65535 || Hkv > 65535) return NEO_ERR_UNSUPPORTED;
+
+    const int tok_per_tile = kBlockM / G;
+    const uint64_t row = 128 * 2;   // bytes per head row
+    CUtensorMap tq, to, tki, tvi, tkp, tvp;
+    {
+        const uint64_t dims[4] = {128, (uint64_t)Hq, (uint64_t)N, (uint64_t)B};
+        const uint64_t strides[3] = {row, row * Hq, row * Hq * N};
+        const uint32_t box[4] = {64, (uint32_t)G, (uint32_t)tok_per_tile, 1};
+        if (!make_map(&tq, q_img, 4, dims, strides, box) || !make_map(&to, out, 4, dims, strides, box))
+            return NEO_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[4] = {128, (uint64_t)Hkv, (uint64_t)N, (uint64_t)B};
+        const uint64_t strides[3] = {row, row * Hkv, row * Hkv * N};
+        const uint32_t box[4] = {64, 1, (uint32_t)kBlockN, 1};
+        if (!make_map(&tki, k_img, 4, dims, strides, box) || !make_map(&tvi, v_img, 4, dims, strides, box))
+            return NEO_ERR_CUDA;
+    }
+    {
+        // With no prefix rows at all the prefix maps are never read; point them at the image keys.
+        const bool empty = total_prefix == 0;
+        const uint64_t dims[3] = {128, (uint64_t)Hkv, empty ? 1 : (uint64_t)total_prefix};
+        const uint64_t strides[2] = {row, row * Hkv};
+        const uint32_t box[3] = {64, 1, (uint32_t)kBlockN};
+        if (!make_map(&tkp, empty ? k_img : k_prefix, 3, dims, strides, box) ||
+            !make_map(&tvp, empty ? v_img : v_prefix, 3, dims, strides, box))
+            return NEO_ERR_CUDA;
+    }
+
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(gen_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
+
+    AttnParams prm;
+    prm.cu_prefix = cu_prefix;
+    prm.lse = lse;
+    prm.total_prefix = total_prefix;
+    prm.B = B;
+    prm.N = N;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = G;
+    prm.tok_per_tile = tok_per_tile;
+    prm.max_prefix = max_prefix;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+
+    const dim3 grid((unsigned)((N + tok_per_tile - 1) / tok_per_tile), (unsigned)Hkv, (unsigned)B);
+    gen_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
+    return neo::launch_status();
+}

@@ -1,0 +1,188 @@
+"""Python binding of libneo: argument marshalling over ctypes, nothing else.
+
+Each function has the name and the argument order of the C entry point
+declared in include/neo.h; tensors are torch CUDA tensors whose device
+pointers are passed through, and the launch goes on torch's current stream
+unless ``stream`` is given. A non-OK status raises NeoError. There is no
+fallback: if libneo.so is missing the first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libneo.so")
+
+NEO_OK, NEO_ERR_INVALID_ARG, NEO_ERR_UNSUPPORTED, NEO_ERR_CUDA, NEO_ERR_TIMEOUT, NEO_ERR_DEVICE = range(6)
+NEO_BF16, NEO_F32 = 0, 1
+NEO_MASK_FULL, NEO_MASK_BLOCK_CAUSAL = 0, 1
+NEO_SEG_TEXT, NEO_SEG_IMAGE = 0, 1
+NEO_DEVERR_TIMEOUT, NEO_DEVERR_BAD_PREFIX = 0x1, 0x2
+
+EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
+           "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version")
+
+
+class NeoError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class neo_pos_segment(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("a", ctypes.c_int32), ("b", ctypes.c_int32), ("c", ctypes.c_int32)]
+
+
+_lib = None
+_vp, _i32, _i64, _f32, _u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_uint64
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libneo.so once and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"libneo.so not found at {path}; build it with "
+                                "attention_neo_qknorm_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    c_int = ctypes.c_int
+    lib.neo_build_positions.argtypes = [_vp, _i64, ctypes.POINTER(neo_pos_segment), c_int, _vp]
+    lib.neo_qknorm_rope3.argtypes = [_vp, _vp, c_int, _i64, c_int, c_int, c_int, _vp, _vp, _vp, _vp, _vp,
+                                     _f32, _f32, _f32, _vp]
+    lib.neo_gen_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, c_int, _vp, _i64, _i32, c_int, c_int, c_int,
+                                      c_int, c_int, c_int, _vp, _vp, _f32, _vp, _vp, _vp]
+    lib.neo_flow_euler_step.argtypes = [_vp, _vp, _i64, _f32, _f32, _f32, _vp, _vp]
+    lib.neo_status_string.argtypes = [c_int]
+    lib.neo_status_string.restype = ctypes.c_char_p
+    lib.neo_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.neo_set_wait_timeout_ns.argtypes = [_u64]
+    lib.neo_version.argtypes = []
+    for name in ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
+                 "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version"):
+        getattr(lib, name).restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().neo_status_string(int(status)).decode()
+    except FileNotFoundError:
+        return f"status {status}"
+
+
+def _check(status: int, what: str):
+    if status != NEO_OK:
+        raise NeoError(status, what)
+
+
+def _stream(stream, t=None):
+    if stream is None:
+        dev = t.device if (t is not None and t.is_cuda) else None
+        return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_DT = {torch.bfloat16: NEO_BF16, torch.float32: NEO_F32}
+
+
+def neo_build_positions(indexes: torch.Tensor, segments, stream=None):
+    """Fill ``indexes`` (int32 [3, S]) from a list of segments
+    ("text", start, count) / ("image", t_index, rows, cols)."""
+    segs = (neo_pos_segment * max(1, len(segments)))()
+    for i, s in enumerate(segments):
+        if s[0] == "text":
+            segs[i] = neo_pos_segment(NEO_SEG_TEXT, int(s[1]), int(s[2]), 0)
+        elif s[0] == "image":
+            segs[i] = neo_pos_segment(NEO_SEG_IMAGE, int(s[1]), int(s[2]), int(s[3]))
+        else:
+            raise ValueError(f"unknown segment {s!r}")
+    S = indexes.shape[1]
+    _check(load_library().neo_build_positions(_ptr(indexes, torch.int32, "indexes"), S, segs, len(segments),
+                                              _stream(stream, indexes)), "neo_build_positions")
+
+
+def neo_qknorm_rope3(q, k, indexes, q_norm_w, q_norm_hw_w, k_norm_w, k_norm_hw_w,
+                     theta_t=5e6, theta_hw=1e4, eps=1e-6, stream=None):
+    """In place: q [S, Hq, 128] and k [S, Hkv, 128] (bf16 or fp32; either may be None)."""
+    ref = q if q is not None else k
+    dt = _DT.get(ref.dtype)
+    if dt is None:
+        raise ValueError("q/k must be bf16 or fp32")
+    S = ref.shape[0]
+    Hq = q.shape[1] if q is not None else 0
+    Hkv = k.shape[1] if k is not None else 0
+    D = ref.shape[2]
+    for t, n in ((q, "q"), (k, "k")):
+        if t is not None and (t.dim() != 3 or t.shape[0] != S or t.dtype != ref.dtype):
+            raise ValueError(f"{n} must be [S, H, 128] of one dtype")
+    _check(load_library().neo_qknorm_rope3(
+        _ptr(q, what="q"), _ptr(k, what="k"), dt, S, Hq, Hkv, D, _ptr(indexes, torch.int32, "indexes"),
+        _ptr(q_norm_w, torch.float32, "q_norm_w") if q is not None else None,
+        _ptr(q_norm_hw_w, torch.float32, "q_norm_hw_w") if q is not None else None,
+        _ptr(k_norm_w, torch.float32, "k_norm_w") if k is not None else None,
+        _ptr(k_norm_hw_w, torch.float32, "k_norm_hw_w") if k is not None else None,
+        float(theta_t), float(theta_hw), float(eps), _stream(stream, ref)), "neo_qknorm_rope3")
+
+
+def neo_gen_attention(q_img, k_prefix, v_prefix, k_img, v_img, cu_prefix, max_prefix, out,
+                      scale=128 ** -0.5, mask_mode=NEO_MASK_FULL, t_prefix=None, t_img=None, lse=None,
+                      stream=None):
+    """out [B, N, Hq, 128] bf16 <- attention of q_img over [prefix ; image] keys."""
+    B, N, Hq, D = q_img.shape
+    Hkv = k_img.shape[2]
+    total_prefix = k_prefix.shape[0] if k_prefix is not None else 0
+    dt = _DT.get(q_img.dtype)
+    if dt is None:
+        raise ValueError("q_img must be bf16")
+    _check(load_library().neo_gen_attention(
+        _ptr(q_img, what="q_img"), _ptr(k_prefix if total_prefix else None, what="k_prefix"),
+        _ptr(v_prefix if total_prefix else None, what="v_prefix"), _ptr(k_img, what="k_img"),
+        _ptr(v_img, what="v_img"), dt, _ptr(cu_prefix, torch.int32, "cu_prefix"), int(total_prefix),
+        int(max_prefix), B, N, Hq, Hkv, D, int(mask_mode), _ptr(t_prefix, torch.int32, "t_prefix"),
+        _ptr(t_img, torch.int32, "t_img"), float(scale), _ptr(out, what="out"),
+        _ptr(lse, torch.float32, "lse"), _stream(stream, q_img)), "neo_gen_attention")
+
+
+def neo_flow_euler_step(z, x0_hat, t, t_next, t_eps=0.02, v_out=None, stream=None):
+    """In place: z <- z + (t_next - t) * (x0_hat - z) / max(1 - t, t_eps) (fp32)."""
+    n = z.numel()
+    if x0_hat.numel() != n or (v_out is not None and v_out.numel() != n):
+        raise ValueError("z, x0_hat and v_out must have the same number of elements")
+    _check(load_library().neo_flow_euler_step(
+        _ptr(z, torch.float32, "z"), _ptr(x0_hat, torch.float32, "x0_hat"), n, float(t), float(t_next),
+        float(t_eps), _ptr(v_out, torch.float32, "v_out"), _stream(stream, z)), "neo_flow_euler_step")
+
+
+def neo_get_device_error(stream=None) -> tuple[int, int]:
+    """(status, word): synchronises the stream, reads and clears the device error word."""
+    word = ctypes.c_uint32(0)
+    st = load_library().neo_get_device_error(_stream(stream), ctypes.byref(word))
+    return st, word.value
+
+
+def neo_set_wait_timeout_ns(ns: int):
+    _check(load_library().neo_set_wait_timeout_ns(int(ns)), "neo_set_wait_timeout_ns")
+
+
+def neo_version() -> int:
+    return load_library().neo_version()

@@ -1,0 +1,71 @@
+"""One generation-pass layer's hot path as a sequence of libneo calls.
+
+Plumbing only: device buffers (torch) and the order of the C-ABI calls.
+Every step runs in a libneo kernel.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import neo, synth
+
+SCALE = 128 ** -0.5
+
+
+def image_segments(w: synth.Workload):
+    return [s for b in range(w.B) for s in w.image_segments(b)]
+
+
+def prefix_segments(w: synth.Workload):
+    return [s for segs in w.prefix_segments for s in segs]
+
+
+class GenPassLayer:
+    """Device buffers of one workload and the hot-path step.
+
+    The frozen prefix cache is produced on construction the way the
+    understanding pass writes it: the raw prefix keys go through the QK-norm
+    and the three-axis RoPE with the prefix positions and the understanding
+    branch's norm weights; the prefix values are stored unchanged.
+    """
+
+    def __init__(self, w: synth.Workload, inp: synth.Inputs, device="cuda", z=None, x0=None):
+        self.w = w
+        d = device
+        self.q = inp.q.to(d).reshape(w.B * w.N, w.Hq, w.D).contiguous()
+        self.k = inp.k.to(d).reshape(w.B * w.N, w.Hkv, w.D).contiguous()
+        self.v = inp.v.to(d).contiguous()
+        self.k_prefix = inp.k_prefix_raw.to(d).contiguous()
+        self.v_prefix = inp.v_prefix.to(d).contiguous()
+        self.wts = [t.to(d) for t in (inp.q_norm, inp.q_norm_hw, inp.k_norm, inp.k_norm_hw,
+                                      inp.k_norm_und, inp.k_norm_hw_und)]
+        self.cu = torch.from_numpy(w.cu_prefix).to(d)
+        self.idx_img = torch.empty(3, w.B * w.N, dtype=torch.int32, device=d)
+        neo.neo_build_positions(self.idx_img, image_segments(w))
+        self.out = torch.empty(w.B, w.N, w.Hq, w.D, dtype=torch.bfloat16, device=d)
+        self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=d)
+        self.max_prefix = max(w.prefix_lens) if w.prefix_lens else 0
+        if w.total_prefix > 0:
+            self.idx_pre = torch.empty(3, w.total_prefix, dtype=torch.int32, device=d)
+            neo.neo_build_positions(self.idx_pre, prefix_segments(w))
+            neo.neo_qknorm_rope3(None, self.k_prefix, self.idx_pre, None, None, self.wts[4], self.wts[5])
+        self.z = z.to(d).contiguous() if z is not None else None
+        self.x0 = x0.to(d).contiguous() if x0 is not None else None
+
+    def norm_rope(self, stream=None):
+        neo.neo_qknorm_rope3(self.q, self.k, self.idx_img, *self.wts[:4], stream=stream)
+
+    def attention(self, lse=True, stream=None):
+        w = self.w
+        neo.neo_gen_attention(self.q.view(w.B, w.N, w.Hq, w.D), self.k_prefix, self.v_prefix,
+                              self.k.view(w.B, w.N, w.Hkv, w.D), self.v, self.cu, self.max_prefix, self.out,
+                              scale=SCALE, lse=self.lse if lse else None, stream=stream)
+
+    def euler(self, t, t_next, t_eps=0.02, stream=None):
+        neo.neo_flow_euler_step(self.z, self.x0, t, t_next, t_eps, stream=stream)
+
+    def step(self, t, t_next, stream=None):
+        self.norm_rope(stream)
+        self.attention(lse=False, stream=stream)
+        self.euler(t, t_next, stream=stream)

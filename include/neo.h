@@ -1,0 +1,182 @@
+/*
+ * libneo: the generation-pass hot path of NEO-unify (SenseNova-U1.5) on one
+ * GB300 GPU (sm_103a), as a plain C ABI.
+ *
+ * Sources of the operations (page title, section):
+ *   [U15] "SenseNova-U1.5 (NEO-unify) architecture"
+ *   [U1]  "SenseNova-U1: Unifying Multimodal Understanding and Generation
+ *          with NEO-unify Architecture"
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor argument is a DEVICE pointer owned by the caller; the
+ *     library never frees, keeps or allocates caller memory. Layouts are
+ *     row-major and contiguous, in the flash-attention [B, S, H, D] order
+ *     ([U1] section 4.4, KV-cache reuse). Tensor pointers must be 16-byte aligned.
+ *   - Work is enqueued on `stream` and runs asynchronously; no entry point
+ *     synchronises the device except neo_get_device_error.
+ *   - Arguments are checked on the host before anything is enqueued. A bad
+ *     argument returns NEO_ERR_INVALID_ARG, a valid but unimplemented case
+ *     NEO_ERR_UNSUPPORTED, a CUDA launch failure NEO_ERR_CUDA; nothing is
+ *     enqueued in those cases. Device-side faults that a host check cannot
+ *     see (an inconsistent cu_prefix array, a pipeline wait that ran out of
+ *     time) are recorded in a device error word read by neo_get_device_error.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef NEO_H
+#define NEO_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NEO_OK = 0,
+    NEO_ERR_INVALID_ARG = 1,
+    NEO_ERR_UNSUPPORTED = 2,
+    NEO_ERR_CUDA = 3,
+    NEO_ERR_TIMEOUT = 4,
+    NEO_ERR_DEVICE = 5
+} neo_status;
+
+typedef enum { NEO_BF16 = 0, NEO_F32 = 1 } neo_dtype;
+
+typedef enum { NEO_MASK_FULL = 0, NEO_MASK_BLOCK_CAUSAL = 1 } neo_mask;
+
+/* Device error word bits (neo_get_device_error). */
+#define NEO_DEVERR_TIMEOUT     0x1u  /* a pipeline wait exceeded its time limit */
+#define NEO_DEVERR_BAD_PREFIX  0x2u  /* cu_prefix not ascending / beyond total_prefix / above max_prefix */
+
+/* ------------------------------------------------------------------------
+ * Position indexes (three rotary axes).
+ * [U15] section "Three rotary axes", last paragraph: all tokens of one image
+ * share one temporal index and their height/width indices tile the token
+ * grid; each CFG branch derives the image's temporal index from its own
+ * prompt length ([U15] section "Runtime / metadata status").
+ *
+ * A sequence is described as consecutive segments:
+ *   kind NEO_SEG_TEXT : a = first position p0, b = count; token i -> (p0+i, p0+i, p0+i)
+ *   kind NEO_SEG_IMAGE: a = temporal index T, b = rows, c = cols; token
+ *                       r*cols + c (row-major) -> (T, r, c)
+ * ------------------------------------------------------------------------ */
+#define NEO_SEG_TEXT 0
+#define NEO_SEG_IMAGE 1
+#define NEO_MAX_SEGMENTS 64
+
+typedef struct {
+    int32_t kind;
+    int32_t a;
+    int32_t b;
+    int32_t c;
+} neo_pos_segment;
+
+/* Writes indexes[3, S] (int32, device, row k = axis k) for the concatenation
+ * of `n_segs` segments (host array, 1..NEO_MAX_SEGMENTS) whose token counts
+ * sum to S. Returns NEO_ERR_INVALID_ARG if the counts do not sum to S, a
+ * segment has a negative size or unknown kind, or indexes is NULL. */
+neo_status neo_build_positions(int32_t* indexes, int64_t S,
+                               const neo_pos_segment* segs, int n_segs,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * QK-norm on head halves, then three-axis RoPE, in place.
+ * [U15] section "Three rotary axes": q_norm/k_norm (weight [64]) normalise
+ * head dims [0:64), q_norm_hw/k_norm_hw dims [64:128); then dims [0:64)
+ * rotate with base theta_t (rope_theta, 5e6) at position indexes[0],
+ * [64:96) with base theta_hw (rope_theta_hw, 1e4) at indexes[1] and
+ * [96:128) with theta_hw at indexes[2]. Each half is
+ *   y = x / sqrt(mean(x^2) + eps) * w,
+ * and each slice of width d at offset o pairs dims (o+i, o+i+d/2),
+ * i < d/2, turning the pair by the angle p * theta^(-2i/d):
+ *   (u, w) -> (u cos a - w sin a, w cos a + u sin a).
+ *
+ * q: [S, Hq, D] and k: [S, Hkv, D] of `dtype` (bf16 or fp32), overwritten
+ * with the result; arithmetic in fp32, one rounding to `dtype` at the end.
+ * Either tensor may be NULL with its head count 0 (e.g. keys only).
+ * indexes: int32 [3, S]. Norm weights: fp32 [64] each; the q weights may be
+ * NULL when Hq == 0 and the k weights when Hkv == 0. D must be 128.
+ * ------------------------------------------------------------------------ */
+neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype,
+                            int64_t S, int Hq, int Hkv, int D,
+                            const int32_t* indexes,
+                            const float* q_norm_w, const float* q_norm_hw_w,
+                            const float* k_norm_w, const float* k_norm_hw_w,
+                            float theta_t, float theta_hw, float eps,
+                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Generation-pass attention over the frozen prefix plus the image tokens.
+ * [U15] section "Mixture of Transformers", items 1-2: the noisy image tokens
+ * attend over the keys/values that the understanding pass wrote for the
+ * prefix, together with their own keys/values, and the cache is not written
+ * (update_cache=False). [U15] section "GQA fusion does not apply": the
+ * generation pass is unmasked (mask_mode NEO_MASK_FULL). For each sequence b
+ * and query head h, with KV head kv = h / (Hq/Hkv):
+ *   out[b,n,h,:] = sum_j softmax_j(scale * <q[b,n,h,:], key_j>) * value_j
+ * over the keys [k_prefix rows of b ; k_img[b,:,kv,:]] (and values alike).
+ *
+ * q_img: [B, N, Hq, D] bf16; k_img, v_img: [B, N, Hkv, D] bf16.
+ * k_prefix, v_prefix: [total_prefix, Hkv, D] bf16, the prefixes of all
+ *   sequences packed without padding; sequence b owns rows
+ *   cu_prefix[b] .. cu_prefix[b+1]-1. NULL allowed when total_prefix == 0.
+ * cu_prefix: int32 [B+1] on the device, cu_prefix[0] = 0, non-decreasing,
+ *   cu_prefix[B] <= total_prefix, every length <= max_prefix (checked on
+ *   the device: a violation sets NEO_DEVERR_BAD_PREFIX and the affected
+ *   sequence's output is left unwritten). A length of 0 is allowed.
+ * D must be 128; Hq must be a multiple of Hkv and 128 a multiple of Hq/Hkv.
+ * mask_mode: NEO_MASK_FULL. NEO_MASK_BLOCK_CAUSAL ([U15] section
+ *   "Block-causal attention") needs t_prefix [total_prefix] and t_img [B*N]
+ *   (int32 temporal indexes) and currently returns NEO_ERR_UNSUPPORTED.
+ * scale: logit scale (1/sqrt(128) in the model), finite and >= 0.
+ * out: [B, N, Hq, D] bf16. lse: optional fp32 [B, Hq, N] natural-log
+ *   sum of exp(logits) per query row, or NULL.
+ * ------------------------------------------------------------------------ */
+neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
+                             const void* v_prefix, const void* k_img,
+                             const void* v_img, neo_dtype dtype,
+                             const int32_t* cu_prefix, int64_t total_prefix,
+                             int32_t max_prefix, int B, int N, int Hq, int Hkv,
+                             int D, neo_mask mask_mode,
+                             const int32_t* t_prefix, const int32_t* t_img,
+                             float scale, void* out, float* lse,
+                             cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * x0 -> velocity conversion and one Euler step, in place.
+ * [U15] section "Flow matching without a VAE": the pixel head predicts x0
+ * and the sampler forms v = (x0 - z) / max(1 - t, t_eps), then
+ * z = z + (t_next - t) * v; t_eps is 0.02 at inference ([U15] section
+ * "Dead or misleading upstream details"). Elementwise, so patch and pixel
+ * layouts give the same result.
+ *
+ * z: fp32 [n], updated in place; x0_hat: fp32 [n]; v_out: optional fp32 [n]
+ * receiving v, or NULL. fp32 arithmetic with a correctly rounded division.
+ * ------------------------------------------------------------------------ */
+neo_status neo_flow_euler_step(float* z, const float* x0_hat, int64_t n,
+                               float t, float t_next, float t_eps,
+                               float* v_out, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* neo_status_string(neo_status s);
+
+/* Synchronises `stream`, then returns the device error word accumulated by
+ * earlier launches in *word (NEO_DEVERR_* bits) and clears it. Returns
+ * NEO_ERR_TIMEOUT if the timeout bit was set, NEO_ERR_DEVICE for any other
+ * bit, NEO_OK if the word was zero, NEO_ERR_CUDA on a CUDA failure.
+ * `word` may be NULL. */
+neo_status neo_get_device_error(cudaStream_t stream, uint32_t* word);
+
+/* Sets the time limit of every pipeline wait inside the kernels, in
+ * nanoseconds (default 1e9). Applies to launches enqueued afterwards. */
+neo_status neo_set_wait_timeout_ns(uint64_t ns);
+
+/* ABI version of this header (major * 100 + minor). */
+int neo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NEO_H */

@@ -8,3 +8,19 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libneo")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def gpu_lib():
+    """Builds (if stale) and loads libneo; a GPU test fails loudly without either."""
+    import torch
+
+    from attention_neo_qknorm_gb300 import neo
+    from attention_neo_qknorm_gb300.build import build
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build()
+    return neo.load_library()

@@ -1,0 +1,119 @@
+"""The C-ABI library builds, loads, exports every entry point declared in
+include/neo.h, and rejects bad arguments on the host before touching a GPU.
+No GPU: every call here returns before any CUDA API call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_neo_qknorm_gb300 import neo
+from attention_neo_qknorm_gb300.build import INCLUDE, build
+
+HEADER = os.path.join(INCLUDE, "neo.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return neo.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(neo_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for required in ("neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), f"libneo.so does not export {name}"
+    assert set(neo.EXPORTS) <= set(names)
+
+
+def test_status_strings_and_version(lib):
+    assert neo.neo_version() == 100
+    for st in range(6):
+        assert lib.neo_status_string(st).decode().startswith("NEO_")
+
+
+V = ctypes.c_void_p
+FAKE = V(0x10000)          # aligned, never dereferenced: the checks fail first
+MISALIGNED = V(0x10008)
+
+
+def _attn(lib, **kw):
+    a = dict(q=FAKE, kp=FAKE, vp=FAKE, ki=FAKE, vi=FAKE, dt=neo.NEO_BF16, cu=FAKE, total=10, maxp=10,
+             B=1, N=64, Hq=32, Hkv=8, D=128, mask=0, tp=None, ti=None, scale=0.088, out=FAKE,
+             lse=None, stream=None)
+    a.update(kw)
+    return lib.neo_gen_attention(a["q"], a["kp"], a["vp"], a["ki"], a["vi"], a["dt"], a["cu"], a["total"],
+                                 a["maxp"], a["B"], a["N"], a["Hq"], a["Hkv"], a["D"], a["mask"], a["tp"],
+                                 a["ti"], a["scale"], a["out"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), neo.NEO_ERR_INVALID_ARG),
+    (dict(Hq=30, Hkv=8), neo.NEO_ERR_INVALID_ARG),
+    (dict(N=0), neo.NEO_ERR_INVALID_ARG),
+    (dict(B=0), neo.NEO_ERR_INVALID_ARG),
+    (dict(q=None), neo.NEO_ERR_INVALID_ARG),
+    (dict(out=None), neo.NEO_ERR_INVALID_ARG),
+    (dict(cu=None), neo.NEO_ERR_INVALID_ARG),
+    (dict(kp=None), neo.NEO_ERR_INVALID_ARG),
+    (dict(q=MISALIGNED), neo.NEO_ERR_INVALID_ARG),
+    (dict(vp=MISALIGNED), neo.NEO_ERR_INVALID_ARG),
+    (dict(scale=-1.0), neo.NEO_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), neo.NEO_ERR_INVALID_ARG),
+    (dict(total=-1), neo.NEO_ERR_INVALID_ARG),
+    (dict(mask=7), neo.NEO_ERR_INVALID_ARG),
+    (dict(dt=neo.NEO_F32), neo.NEO_ERR_UNSUPPORTED),
+    (dict(Hq=3, Hkv=1), neo.NEO_ERR_UNSUPPORTED),
+])
+def test_attention_rejects_bad_arguments(lib, kw, status):
+    assert _attn(lib, **kw) == status
+
+
+def test_qknorm_rope3_rejects_bad_arguments(lib):
+    f = lib.neo_qknorm_rope3
+    args = [FAKE, FAKE, neo.NEO_BF16, 16, 4, 1, 128, FAKE, FAKE, FAKE, FAKE, FAKE, 5e6, 1e4, 1e-6, None]
+    bad = {6: 64, 2: 9, 0: MISALIGNED, 8: None, 12: -1.0, 14: float("inf"), 3: -5}
+    for pos, val in bad.items():
+        a = list(args)
+        a[pos] = val
+        assert f(*a) == neo.NEO_ERR_INVALID_ARG, pos
+    a = list(args)
+    a[3] = 0                        # S == 0: nothing to do
+    assert f(*a) == neo.NEO_OK
+    a = list(args)
+    a[7] = None                     # indexes missing
+    assert f(*a) == neo.NEO_ERR_INVALID_ARG
+
+
+def test_euler_rejects_bad_arguments(lib):
+    f = lib.neo_flow_euler_step
+    assert f(FAKE, FAKE, 0, 0.5, 0.6, 0.02, None, None) == neo.NEO_OK
+    assert f(None, FAKE, 8, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(MISALIGNED, FAKE, 8, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 8, 1.0, 1.1, 0.0, None, None) == neo.NEO_ERR_INVALID_ARG   # max(1-t, t_eps) = 0
+    assert f(FAKE, FAKE, 8, float("nan"), 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+
+
+def test_positions_rejects_bad_segments(lib):
+    Seg = neo.neo_pos_segment
+    segs = (Seg * 2)(Seg(neo.NEO_SEG_TEXT, 0, 4, 0), Seg(neo.NEO_SEG_IMAGE, 4, 2, 3))
+    f = lib.neo_build_positions
+    assert f(FAKE, 9, segs, 2, None) == neo.NEO_ERR_INVALID_ARG      # counts sum to 10
+    assert f(None, 10, segs, 2, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(FAKE, 10, segs, 0, None) == neo.NEO_ERR_INVALID_ARG
+    bad = (Seg * 1)(Seg(5, 0, 1, 1))
+    assert f(FAKE, 1, bad, 1, None) == neo.NEO_ERR_INVALID_ARG

@@ -1,0 +1,94 @@
+"""GPU parity of neo_gen_attention against the fp64 oracle on identical bf16
+inputs: several tiles, ragged prefixes and image tails, empty prefixes, GQA
+group sizes, the log-sum-exp output, and device-side prefix checks."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from attention_neo_qknorm_gb300 import neo
+from helpers import SCALE, assert_bf16_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(prefix, N, Hq, Hkv, seed=0, scale=SCALE, lse=True):
+    B = len(prefix)
+    g = torch.Generator().manual_seed(seed)
+    bf = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+    total = int(sum(prefix))
+    q, k, v = bf(B, N, Hq, 128), bf(B, N, Hkv, 128), bf(B, N, Hkv, 128)
+    kp, vp = bf(total, Hkv, 128), bf(total, Hkv, 128)
+    cu = np.concatenate([[0], np.cumsum(prefix)]).astype(np.int32)
+    out = torch.full((B, N, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse_d = torch.full((B, Hq, N), float("nan"), device="cuda") if lse else None
+    neo.neo_gen_attention(q.cuda(), kp.cuda() if total else None, vp.cuda() if total else None, k.cuda(),
+                          v.cuda(), torch.from_numpy(cu).cuda(), max(prefix), out, scale=scale, lse=lse_d)
+    ref, ref_lse = O.gen_attention(f64(q), f64(kp), f64(vp), f64(k), f64(v), cu, scale)
+    assert_bf16_close(f64(out), ref, f"out prefix={prefix} N={N} {Hq}/{Hkv}")
+    if lse:
+        np.testing.assert_allclose(f64(lse_d), ref_lse, rtol=1e-4, atol=1e-3)
+    return out
+
+
+@pytest.mark.parametrize("prefix,N,Hq,Hkv", [
+    ((200, 77), 132, 8, 2),        # ragged prefixes and image tail, G = 4
+    ((32,), 64, 4, 1),             # tiny reference shape
+    ((256,), 128, 8, 2),           # exact multiples of the tile
+    ((0, 130), 257, 8, 2),         # an empty prefix; N = 2 tiles + 1 token
+    ((0,), 1, 4, 1),               # a single key: the output is V
+    ((5, 129, 300), 40, 16, 2),    # G = 8, three sequences
+    ((130,), 100, 2, 2),           # G = 1 (plain multi-head)
+    ((70,), 90, 4, 2),             # G = 2
+    ((1000,), 384, 32, 8),         # production head counts
+])
+def test_attention_matches_oracle(gpu_lib, prefix, N, Hq, Hkv):
+    run_case(prefix, N, Hq, Hkv, seed=N + Hq)
+
+
+def test_attention_zero_scale_gives_mean_value(gpu_lib):
+    run_case((40,), 50, 4, 1, scale=0.0, seed=5)
+
+
+def test_attention_large_logits(gpu_lib):
+    """A large scale makes the running maximum jump across tiles, exercising
+    the output rescale path."""
+    run_case((300,), 200, 8, 2, scale=0.35, seed=6)
+
+
+def test_attention_without_lse_and_repeated_calls(gpu_lib):
+    a = run_case((150,), 140, 8, 2, seed=8, lse=False)
+    b = run_case((150,), 140, 8, 2, seed=8, lse=False)
+    assert torch.equal(a, b)   # deterministic
+
+
+def test_attention_bad_cu_prefix_sets_device_error(gpu_lib):
+    B, N, Hq, Hkv = 2, 64, 4, 1
+    q = torch.randn(B, N, Hq, 128, device="cuda").to(torch.bfloat16)
+    k = torch.randn(B, N, Hkv, 128, device="cuda").to(torch.bfloat16)
+    kp = torch.randn(40, Hkv, 128, device="cuda").to(torch.bfloat16)
+    out = torch.zeros(B, N, Hq, 128, dtype=torch.bfloat16, device="cuda")
+    neo.neo_get_device_error()   # clear
+    cu = torch.tensor([0, 30, 20], dtype=torch.int32, device="cuda")   # descending
+    neo.neo_gen_attention(q, kp, kp, k, k, cu, 40, out)
+    st, word = neo.neo_get_device_error()
+    assert st == neo.NEO_ERR_DEVICE and word & neo.NEO_DEVERR_BAD_PREFIX
+    cu = torch.tensor([0, 30, 40], dtype=torch.int32, device="cuda")
+    neo.neo_gen_attention(q, kp, kp, k, k, cu, 20, out)                  # length above max_prefix
+    st, word = neo.neo_get_device_error()
+    assert word & neo.NEO_DEVERR_BAD_PREFIX
+    neo.neo_gen_attention(q, kp, kp, k, k, cu, 40, out)                  # consistent again
+    st, word = neo.neo_get_device_error()
+    assert st == neo.NEO_OK and word == 0
+
+
+def test_block_causal_mode_is_reported_unsupported(gpu_lib):
+    q = torch.zeros(1, 8, 4, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16, device="cuda")
+    cu = torch.zeros(2, dtype=torch.int32, device="cuda")
+    t = torch.zeros(8, dtype=torch.int32, device="cuda")
+    with pytest.raises(neo.NeoError) as e:
+        neo.neo_gen_attention(q, None, None, k, k, cu, 0, q.clone(), mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
+                              t_img=t)
+    assert e.value.status == neo.NEO_ERR_UNSUPPORTED

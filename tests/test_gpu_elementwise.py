@@ -1,0 +1,132 @@
+"""GPU parity of the HBM-bound kernels against the fp64 oracle: position
+indexes (exact), QK-norm halves + three-axis RoPE (bf16 and fp32), and the
+x0 -> v Euler step (fp32)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from attention_neo_qknorm_gb300 import neo, synth
+from helpers import F32_TOL, assert_bf16_close, f64, image_segments, max_abs, prefix_segments, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_positions_exact(gpu_lib, name):
+    w = synth.WORKLOADS[name]
+    for segs, S in ((image_segments(w), w.B * w.N), (prefix_segments(w), w.total_prefix)):
+        idx = torch.full((3, S), -7, dtype=torch.int32, device="cuda")
+        neo.neo_build_positions(idx, segs)
+        np.testing.assert_array_equal(idx.cpu().numpy(), O.positions(segs))
+
+
+def _norm_rope_case(S, Hq, Hkv, dtype, segs, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(S, Hq, 128, generator=g).to(dtype)
+    k = torch.randn(S, Hkv, 128, generator=g).to(dtype)
+    ws = [torch.rand(64, generator=g) + 0.5 for _ in range(4)]
+    idx = O.positions(segs)
+    qd, kd = q.cuda(), k.cuda()
+    idx_d = torch.from_numpy(idx.astype(np.int32)).cuda()
+    neo.neo_qknorm_rope3(qd, kd, idx_d, *[t.cuda() for t in ws])
+    rq = O.qknorm_rope3(f64(q), idx, f64(ws[0]), f64(ws[1]))
+    rk = O.qknorm_rope3(f64(k), idx, f64(ws[2]), f64(ws[3]))
+    return f64(qd), rq, f64(kd), rk
+
+
+@pytest.mark.parametrize("segs,Hq,Hkv", [
+    ([("text", 0, 37)], 4, 1),
+    ([("text", 0, 512), ("image", 512, 32, 32)], 32, 8),
+    ([("image", 1024, 64, 64)], 32, 8),
+    ([("image", 6000, 3, 5)], 6, 2),
+])
+def test_qknorm_rope3_bf16(gpu_lib, segs, Hq, Hkv):
+    S = O.positions(segs).shape[1]
+    gq, rq, gk, rk = _norm_rope_case(S, Hq, Hkv, torch.bfloat16, segs, seed=S)
+    assert_bf16_close(gq, rq, "q")
+    assert_bf16_close(gk, rk, "k")
+
+
+def test_qknorm_rope3_fp32(gpu_lib):
+    segs = [("text", 0, 32), ("image", 32, 8, 8)]
+    gq, rq, gk, rk = _norm_rope_case(96, 4, 1, torch.float32, segs, seed=3)
+    # fp32 end to end: only the fp32 angle (|a| up to 95 rad here) and rsqrt limit the error.
+    assert max_abs(gq, rq) < 2e-5 and max_abs(gk, rk) < 2e-5
+
+
+def test_qknorm_rope3_keys_only_and_queries_only(gpu_lib):
+    segs = [("text", 0, 20)]
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(20, 2, 128, generator=g).to(torch.bfloat16)
+    w1, w2 = torch.rand(64, generator=g) + 0.5, torch.rand(64, generator=g) + 0.5
+    idx = torch.from_numpy(O.positions(segs).astype(np.int32)).cuda()
+    ref = O.qknorm_rope3(f64(x), O.positions(segs), f64(w1), f64(w2))
+    kd = x.cuda()
+    neo.neo_qknorm_rope3(None, kd, idx, None, None, w1.cuda(), w2.cuda())
+    assert_bf16_close(f64(kd), ref, "k only")
+    qd = x.cuda()
+    neo.neo_qknorm_rope3(qd, None, idx, w1.cuda(), w2.cuda(), None, None)
+    assert_bf16_close(f64(qd), ref, "q only")
+
+
+def _euler_check(z, x0, t, tn, with_v=True):
+    zd, xd = z.cuda(), x0.cuda()
+    vd = torch.empty_like(zd) if with_v else None
+    neo.neo_flow_euler_step(zd, xd, t, tn, 0.02, vd)
+    rz, rv = O.flow_euler_step(f64(z), f64(x0), np.float32(t), np.float32(tn), np.float32(0.02))
+    assert max_abs(f64(zd), rz) <= F32_TOL * max(1.0, np.abs(rz).max())
+    assert rel_frob(f64(zd), rz) <= F32_TOL
+    if with_v:
+        assert rel_frob(f64(vd), rv) <= F32_TOL
+    return zd
+
+
+@pytest.mark.parametrize("name", ["tiny_ref", "gen_2048"])
+def test_euler_step_matches_oracle(gpu_lib, name):
+    w = synth.WORKLOADS[name]
+    z, (x0,) = synth.make_flow(w)
+    _euler_check(z, x0, w.t_steps[0], w.t_steps[0] + w.dt)
+
+
+def test_euler_ragged_tail_and_t_eps_clamp(gpu_lib):
+    g = torch.Generator().manual_seed(11)
+    for n in (1, 3, 4097, 1000003):
+        z, x0 = torch.randn(n, generator=g), torch.randn(n, generator=g)
+        _euler_check(z, x0, 0.99, 1.0)
+        _euler_check(z, x0, 0.25, 0.35, with_v=False)
+
+
+def test_euler_worked_example(gpu_lib):
+    """t = 0.6, x0 = 1, z = 0.6: v = 1 and the step to 0.7 lands on 0.7."""
+    z = torch.full((8,), 0.6, device="cuda")
+    x0 = torch.ones(8, device="cuda")
+    v = torch.empty(8, device="cuda")
+    neo.neo_flow_euler_step(z, x0, 0.6, 0.7, 0.02, v)
+    assert np.allclose(v.cpu().numpy(), 1.0, atol=1e-6) and np.allclose(z.cpu().numpy(), 0.7, atol=1e-6)
+
+
+def test_euler_ten_steps_ragged_batch_lands_on_x0(gpu_lib):
+    """Ragged CFG workload: ten steps t = 0 .. 0.9 with a fixed x0_hat land on
+    x0_hat (straight-path closed form), at the full 4 x 4096 x 3072 size."""
+    w = synth.WORKLOADS["ragged_cfg"]
+    z, (x0,) = synth.make_flow(w)
+    zd, xd = z.cuda(), x0.cuda()
+    for t in w.t_steps:
+        neo.neo_flow_euler_step(zd, xd, t, t + w.dt, 0.02)
+    assert max_abs(f64(zd), f64(x0)) <= 1e-5 * 8
+
+
+def test_euler_ten_steps_against_oracle(gpu_lib):
+    g = torch.Generator().manual_seed(12)
+    n = 3 * 4096 + 5
+    z = torch.randn(n, generator=g)
+    xs = [torch.randn(n, generator=g) for _ in range(10)]
+    zd = z.cuda()
+    rz = f64(z)
+    for k in range(10):
+        t, tn = np.float32(k / 10), np.float32((k + 1) / 10)
+        neo.neo_flow_euler_step(zd, xs[k].cuda(), float(t), float(tn), 0.02)
+        rz, _ = O.flow_euler_step(rz, f64(xs[k]), t, tn, np.float32(0.02))
+    assert rel_frob(f64(zd), rz) <= F32_TOL

@@ -20,12 +20,20 @@ extern "C" const char* neo_status_string(neo_status s) {
 }
 
 extern "C" neo_status neo_get_device_error(cudaStream_t stream, uint32_t* word) {
-    return neo::attention_error_read_clear(stream, word);
+    uint32_t a = 0, e = 0;
+    neo_status st = neo::attention_error_read_clear(stream, &a);   // synchronises the stream
+    if (st == NEO_ERR_CUDA) return st;
+    if (neo::elementwise_error_read_clear(&e) != NEO_OK) return NEO_ERR_CUDA;
+    const uint32_t all = a | e;
+    if (word) *word = all;
+    if (all & NEO_DEVERR_TIMEOUT) return NEO_ERR_TIMEOUT;
+    return all ? NEO_ERR_DEVICE : NEO_OK;
 }
 
 extern "C" neo_status neo_set_wait_timeout_ns(uint64_t ns) {
     if (ns == 0) return NEO_ERR_INVALID_ARG;
-    return neo::attention_set_timeout(ns);
+    const neo_status st = neo::attention_set_timeout(ns);
+    return st != NEO_OK ? st : neo::elementwise_set_timeout(ns);
 }
 
 extern "C" int neo_version(void) { return 100; }

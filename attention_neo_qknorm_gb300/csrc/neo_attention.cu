@@ -258,25 +258,38 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after();
             float s[128];
             {
-                uint32_t r[32];
+                uint32_t r[128];
+                tmem_ld128(lane_base + kTmS0 + (uint32_t)(j & 1) * 128u, r);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(lane_base + kTmS0 + (uint32_t)(j & 1) * 128u + c * 32u, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-                }
+                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
             }
             tc_fence_before();
             mbar_arrive(bar_addr(sb, BAR_S_FREE + (j & 1)));
 
+            // Keys past the end of the prefix or image segment do not exist.
             const int valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
-            float mx = -INFINITY;
+            const bool partial = valid < kBlockN;
+            if (partial) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                s[c] = c < valid ? s[c] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+                for (int c = 0; c < 128; ++c) s[c] = c < valid ? s[c] : -INFINITY;
             }
-            const float m_new = fmaxf(m_used, mx);
+            // Row maximum of the raw logits: a three-input max tree (depth 5).
+            float mraw;
+            {
+                float t1[43];
+#pragma unroll
+                for (int i = 0; i < 42; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+                t1[42] = fmaxf(s[126], s[127]);
+                float t2[15];
+#pragma unroll
+                for (int i = 0; i < 14; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+                t2[14] = t1[42];
+                float t3[5];
+#pragma unroll
+                for (int i = 0; i < 5; ++i) t3[i] = fmax3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
+                mraw = fmax3(fmax3(t3[0], t3[1], t3[2]), t3[3], t3[4]);
+            }
+            const float m_new = fmaxf(m_used, mraw * p.scale_log2);
             const bool need = m_new > m_used + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ex2(m_used - m_new) : 1.0f;
@@ -298,16 +311,25 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     tmem_st_wait();
                 }
             }
-            float rs = 0.f;
+            // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU,
+            // eight independent partial sums.
+            const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm = make_float2(-m_used, -m_used);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = ex2(s[2 * c] - m_used);
-                const float p1 = ex2(s[2 * c + 1] - m_used);
-                rs += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
+                float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
+                if (partial) {
+                    a.x = 2 * c < valid ? a.x : -INFINITY;
+                    a.y = 2 * c + 1 < valid ? a.y : -INFINITY;
+                }
+                const float2 e = make_float2(ex2(a.x), ex2(a.y));
+                acc[c & 3] = fadd2(acc[c & 3], e);
+                pk[c] = pack_bf16x2(e.x, e.y);
             }
-            l_sum += rs;
+            l_sum += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             if (j >= 2) {
                 // P buffer j&1 was last read by PV_{j-2}.
                 ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u));

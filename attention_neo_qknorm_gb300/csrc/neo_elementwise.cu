@@ -9,12 +9,14 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "neo.h"
 #include "neo_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -62,157 +64,228 @@ __global__ void positions_kernel(int32_t* __restrict__ idx, int64_t S, const Seg
 // ---------------------------------------------------------------------------
 // QK-norm on halves + three-axis RoPE ([U15] "Three rotary axes").
 //
-// A CTA owns kTokensPerCta consecutive tokens and every q and k head row of
-// them. It first builds the (cos, sin) table of the tokens' 64 rotation pairs
-// in shared memory (pairs [0,32) temporal, [32,48) height, [48,64) width;
-// the angle only depends on the token, so each sincos is shared by all
-// Hq + Hkv heads), then streams the rows. Each row of 128 values is handled
-// by 16 lanes with 16-byte accesses (8 bf16 or 4 fp32 per lane: 16 or 32
-// lanes per row). The half's sum of squares is reduced with shuffles; the
-// rotation partner of a lane's values sits d/2 dims away, i.e. a fixed lane
-// xor within the same half, so one shuffle per value brings it over.
+// Work item = one token and up to kHeadsPerItem of its q heads or of its k
+// heads (items never mix the two). A row of 128 values is owned by a group of
+// lanes in which every lane holds BOTH members of its rotation pairs: two
+// 16-byte chunks at dims [a, a+E) and [a+d/2, a+d/2+E) of its slice (E = 8
+// bf16 or 4 fp32), so the rotation needs no data exchange. Lanes [0, 32/E) of
+// the group cover the temporal slice [0,64) (= the first normalised half),
+// the others the height [64,96) and width [96,128) slices (= the second
+// half); the half's sum of squares is a shuffle reduction inside that aligned
+// lane group. Each lane computes the (cos, sin) of its E pairs once per item.
+// The CTAs are persistent; each warp keeps its next kNormDepth - 1 items in
+// flight with cp.async copies into a private shared-memory ring while the
+// current item is normalised, rotated and stored.
 // ---------------------------------------------------------------------------
+__device__ unsigned int g_elem_error = 0;
+__device__ unsigned long long g_elem_wait_limit_ns = 1000000000ull;
+
 struct RopeFreqs {
-    float f[64];   // theta^(-2i/d) per pair, in table order
+    // theta^(-2i/d) of each pair split as hi + lo: hi keeps 11 significant bits
+    // so that pos * hi is exact in fp32 for positions below 2^13.
+    float hi[64];
+    float lo[64];   // pairs [0,32) temporal, [32,48) height, [48,64) width
 };
 
 constexpr int kNormThreads = 256;
-constexpr int kTokensPerCta = 8;
-constexpr int kRowUnroll = 2;
+constexpr int kNormCtasPerSm = 3;
+constexpr int kHeadsPerItem = 4;
+constexpr int kNormDepth = 2;
+
+// sin/cos of pos * f with f = hi + lo: the exact product pos * hi is reduced
+// modulo 2*pi by the two-constant Cody-Waite scheme (2*pi = C1 + C2, each
+// fp32, products folded with fma), then the small product pos * lo is added
+// and the SFU evaluates sin/cos on the reduced argument in [-pi, pi].
+__device__ __forceinline__ void rope_sincos(float pos, float f_hi, float f_lo, float* sn, float* cs) {
+    constexpr float kTwoPiHi = 6.28318548202514648f;        // fp32(2*pi)
+    constexpr float kTwoPiLo = -1.7484556025237907e-07f;    // 2*pi - kTwoPiHi
+    constexpr float kInvTwoPi = 0.15915494309189535f;
+    const float a = pos * f_hi;
+    const float k = rintf(a * kInvTwoPi);
+    float r = fmaf(-k, kTwoPiHi, a);
+    r = fmaf(-k, kTwoPiLo, r);
+    r = fmaf(pos, f_lo, r);
+    __sincosf(r, sn, cs);
+}
 
 template <typename T>
-struct LaneIO;
+struct Chunk;    // one 16-byte chunk of a row
 
 template <>
-struct LaneIO<__nv_bfloat16> {
+struct Chunk<__nv_bfloat16> {
     static constexpr int E = 8;
-    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[8]) {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
+    static __device__ __forceinline__ void unpack(uint4 u, float (&x)[8]) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-            const float2 f = __bfloat1622float2(h);
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
             x[2 * i] = f.x;
             x[2 * i + 1] = f.y;
         }
     }
-    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&y)[8]) {
+    static __device__ __forceinline__ uint4 pack(const float (&y)[8]) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
             w[i] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
 
 template <>
-struct LaneIO<float> {
+struct Chunk<float> {
     static constexpr int E = 4;
-    static __device__ __forceinline__ void load(const float* p, float (&x)[4]) {
-        const float4 u = *reinterpret_cast<const float4*>(p);
-        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    static __device__ __forceinline__ void unpack(uint4 u, float (&x)[4]) {
+        x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
     }
-    static __device__ __forceinline__ void store(float* p, const float (&y)[4]) {
-        *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+    static __device__ __forceinline__ uint4 pack(const float (&y)[4]) {
+        return make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]), __float_as_uint(y[2]), __float_as_uint(y[3]));
     }
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kNormThreads)
+__global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm)
 qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int Hkv,
                     const int32_t* __restrict__ idx,
                     const float* __restrict__ wq_t, const float* __restrict__ wq_hw,
                     const float* __restrict__ wk_t, const float* __restrict__ wk_hw,
-                    const RopeFreqs freqs, float eps) {
-    constexpr int E = LaneIO<T>::E;          // values per lane
-    constexpr int LPR = 128 / E;             // lanes per row
+                    const __grid_constant__ RopeFreqs freqs, float eps, int64_t n_items) {
+    constexpr int E = Chunk<T>::E;
+    constexpr int LPR = 64 / E;              // lanes per row (8 bf16, 16 fp32)
+    constexpr int HALF_LANES = 32 / E;       // lanes per normalised half
     constexpr int ROWS_PER_WARP = 32 / LPR;
-    constexpr int WORKERS = kNormThreads / LPR;
-    constexpr int HALF_LANES = 64 / E;       // lanes per normalised half
 
-    __shared__ float2 cs[kTokensPerCta][64];
-    __shared__ float wq[128];
-    __shared__ float wk[128];
+    __shared__ __align__(16) float w_s[2][128];   // norm weights of the full head dim: q, k
 
-    const int64_t tok0 = (int64_t)blockIdx.x * kTokensPerCta;
-    const int ntok = (int)(S - tok0 < kTokensPerCta ? S - tok0 : kTokensPerCta);
-
-    for (int e = threadIdx.x; e < ntok * 64; e += kNormThreads) {
-        const int t = e >> 6, pr = e & 63;
-        const int axis = pr < 32 ? 0 : (pr < 48 ? 1 : 2);
-        const float pos = (float)idx[axis * S + tok0 + t];
-        float sn, cn;
-        sincosf(pos * freqs.f[pr], &sn, &cn);
-        cs[t][pr] = make_float2(cn, sn);
+    const int lane = threadIdx.x & 31;
+    const int sub = threadIdx.x % LPR;
+    // This lane's slice, first dims of its u and w chunks, first pair (table order).
+    int dim_a, half_w, pair0, axis;
+    if (sub < HALF_LANES) {
+        dim_a = sub * E; half_w = 32; pair0 = sub * E; axis = 0;
+    } else if (sub < HALF_LANES + HALF_LANES / 2) {
+        const int m = sub - HALF_LANES;
+        dim_a = 64 + m * E; half_w = 16; pair0 = 32 + m * E; axis = 1;
+    } else {
+        const int m = sub - HALF_LANES - HALF_LANES / 2;
+        dim_a = 96 + m * E; half_w = 16; pair0 = 48 + m * E; axis = 2;
     }
-    for (int e = threadIdx.x; e < 128; e += kNormThreads) {
-        wq[e] = Hq > 0 ? (e < 64 ? wq_t[e] : wq_hw[e - 64]) : 0.f;
-        wk[e] = Hkv > 0 ? (e < 64 ? wk_t[e] : wk_hw[e - 64]) : 0.f;
+    const int dim_b = dim_a + half_w;
+    float fh[E], fl[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        fh[j] = freqs.hi[pair0 + j];
+        fl[j] = freqs.lo[pair0 + j];
+    }
+    for (int e = threadIdx.x; e < 256; e += kNormThreads) {
+        const int which = e >> 7, d = e & 127;
+        const float* wt = which ? wk_t : wq_t;
+        const float* wh = which ? wk_hw : wq_hw;
+        const bool present = which ? Hkv > 0 : Hq > 0;
+        w_s[which][d] = present ? (d < 64 ? wt[d] : wh[d - 64]) : 0.f;
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int sub = threadIdx.x % LPR;              // lane within the row
-    const int e0 = sub * E;                          // first head dim of this lane
-    const bool temporal = e0 < 64;
-    const int slice_off = temporal ? 0 : (e0 < 96 ? 64 : 96);
-    const int half_w = temporal ? 32 : 16;           // half the slice width
-    const bool first = (e0 - slice_off) < half_w;    // lane holds the u side of its pairs
-    const int pair0 = (temporal ? 0 : (e0 < 96 ? 32 : 48)) + (e0 - slice_off) % half_w;
-    const int partner = lane ^ (half_w / E);
+    // Per token: ceil(Hq/R) q items, then ceil(Hkv/R) k items (R = kHeadsPerItem).
+    // The host guarantees n_items < 2^31.
+    const int q_items = (Hq + kHeadsPerItem - 1) / kHeadsPerItem;
+    const int k_items = (Hkv + kHeadsPerItem - 1) / kHeadsPerItem;
+    const uint32_t per_tok = (uint32_t)(q_items + k_items);
+    const uint32_t n_it = (uint32_t)n_items;
+    const uint32_t first = ((blockIdx.x * kNormThreads + threadIdx.x) >> 5) * ROWS_PER_WARP;
+    const uint32_t stride = ((gridDim.x * kNormThreads) >> 5) * ROWS_PER_WARP;
+    const uint32_t sub_item = (uint32_t)(lane / LPR);
 
-    const int H = Hq + Hkv;
-    const int rows = ntok * H;
-    const int warp_row0 = (threadIdx.x >> 5) * ROWS_PER_WARP;
-    const int my_off = lane / LPR;
+    // Each warp keeps kNormDepth items in flight with cp.async copies into its
+    // own ring of shared-memory slots; a lane copies exactly the chunks it
+    // later reads, so its own wait_group is the only synchronisation needed.
+    constexpr uint32_t SLOT_BYTES = ROWS_PER_WARP * kHeadsPerItem * 128 * sizeof(T);
+    extern __shared__ __align__(16) uint8_t ring_mem[];
+    uint8_t* ring = ring_mem + (size_t)(threadIdx.x >> 5) * kNormDepth * SLOT_BYTES;
+    const uint32_t lane_off = (uint32_t)(lane / LPR) * kHeadsPerItem * 128 * sizeof(T);
 
-    for (int rb = warp_row0; rb < rows; rb += WORKERS * kRowUnroll) {
-        float x[kRowUnroll][E];
-        T* ptr[kRowUnroll];
-        int tok[kRowUnroll];
-        bool active[kRowUnroll];
+    struct Item {
+        T* base;
+        int nh;
+        int is_k;
+        int64_t tok;
+    };
+    auto locate = [&](uint32_t wb) {
+        Item it;
+        const uint32_t item = wb + sub_item;
+        const bool active = item < n_it;
+        it.tok = active ? (int64_t)(item / per_tok) : 0;
+        const int c = active ? (int)(item % per_tok) : 0;
+        it.is_k = c >= q_items;
+        const int h0 = (it.is_k ? c - q_items : c) * kHeadsPerItem;
+        it.nh = active ? min(kHeadsPerItem, (it.is_k ? Hkv : Hq) - h0) : 0;
+        it.base = it.is_k ? k + (it.tok * Hkv + h0) * 128 : q + (it.tok * Hq + h0) * 128;
+        return it;
+    };
+    auto issue = [&](uint32_t wb, int slot) {
+        const Item it = locate(wb);
+        const uint32_t dst = sm103::smem_addr(ring + (size_t)slot * SLOT_BYTES + lane_off);
 #pragma unroll
-        for (int u = 0; u < kRowUnroll; ++u) {
-            const int r = rb + u * WORKERS + my_off;
-            active[u] = r < rows;
-            const int t = active[u] ? r / H : 0;
-            const int h = active[u] ? r % H : 0;
-            tok[u] = t;
-            ptr[u] = h < Hq ? q + ((tok0 + t) * Hq + h) * 128 + e0
-                            : k + ((tok0 + t) * Hkv + (h - Hq)) * 128 + e0;
-            if (active[u]) {
-                LaneIO<T>::load(ptr[u], x[u]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < E; ++j) x[u][j] = 0.f;
+        for (int r = 0; r < kHeadsPerItem; ++r) {
+            if (r < it.nh) {
+                const uint32_t d = dst + (uint32_t)r * 128u * sizeof(T);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + dim_a * (uint32_t)sizeof(T)),
+                             "l"(it.base + r * 128 + dim_a) : "memory");
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + dim_b * (uint32_t)sizeof(T)),
+                             "l"(it.base + r * 128 + dim_b) : "memory");
             }
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto process = [&](uint32_t wb, int slot) {
+        const Item it = locate(wb);
+        const float pos = it.nh > 0 ? (float)__ldg(idx + axis * S + it.tok) : 0.f;
+        float cs[E], sn[E];
 #pragma unroll
-        for (int u = 0; u < kRowUnroll; ++u) {
-            const int r = rb + u * WORKERS + my_off;
-            const float* w = (active[u] && (r % H) < Hq) ? wq : wk;
+        for (int j = 0; j < E; ++j) rope_sincos(pos, fh[j], fl[j], &sn[j], &cs[j]);
+        const uint8_t* src = ring + (size_t)slot * SLOT_BYTES + lane_off;
+#pragma unroll
+        for (int r = 0; r < kHeadsPerItem; ++r) {
+            const uint8_t* rowp = src + r * 128 * sizeof(T);
+            const uint4 ua = *reinterpret_cast<const uint4*>(rowp + dim_a * sizeof(T));
+            const uint4 ub = *reinterpret_cast<const uint4*>(rowp + dim_b * sizeof(T));
+            float xa[E], xb[E];
+            Chunk<T>::unpack(ua, xa);
+            Chunk<T>::unpack(ub, xb);
             float ss = 0.f;
 #pragma unroll
-            for (int j = 0; j < E; ++j) ss = fmaf(x[u][j], x[u][j], ss);
+            for (int j = 0; j < E; ++j) ss = fmaf(xa[j], xa[j], fmaf(xb[j], xb[j], ss));
 #pragma unroll
             for (int m = 1; m < HALF_LANES; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
             const float rs = rsqrtf(ss * (1.0f / 64.0f) + eps);
-            float y[E], yp[E], o[E];
-#pragma unroll
-            for (int j = 0; j < E; ++j) y[j] = x[u][j] * rs * w[e0 + j];
-#pragma unroll
-            for (int j = 0; j < E; ++j) yp[j] = __shfl_sync(0xffffffffu, y[j], partner);
+            float ya[E], yb[E];
 #pragma unroll
             for (int j = 0; j < E; ++j) {
-                const float2 c = cs[tok[u]][pair0 + j];
-                o[j] = first ? fmaf(y[j], c.x, -yp[j] * c.y) : fmaf(y[j], c.x, yp[j] * c.y);
+                const float u = xa[j] * rs * w_s[it.is_k][dim_a + j];
+                const float w = xb[j] * rs * w_s[it.is_k][dim_b + j];
+                ya[j] = fmaf(u, cs[j], -w * sn[j]);
+                yb[j] = fmaf(w, cs[j], u * sn[j]);
             }
-            if (active[u]) LaneIO<T>::store(ptr[u], o);
+            if (r < it.nh) {
+                *reinterpret_cast<uint4*>(it.base + r * 128 + dim_a) = Chunk<T>::pack(ya);
+                *reinterpret_cast<uint4*>(it.base + r * 128 + dim_b) = Chunk<T>::pack(yb);
+            }
         }
+    };
+
+#pragma unroll
+    for (int d = 0; d < kNormDepth; ++d) issue(first + (uint32_t)d * stride, d);
+    int slot = 0;
+    for (uint32_t wb = first; wb < n_it; wb += stride) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kNormDepth - 1) : "memory");
+        process(wb, slot);
+        issue(wb + (uint32_t)kNormDepth * stride, slot);   // the slot was just read by this lane only
+        slot = slot + 1 == kNormDepth ? 0 : slot + 1;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -268,6 +341,23 @@ flow_euler_kernel(float* __restrict__ z, const float* __restrict__ x0, int64_t n
 
 }  // namespace
 
+namespace neo {
+
+neo_status elementwise_error_read_clear(uint32_t* word) {
+    unsigned int h = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&h, g_elem_error, sizeof(h)) != cudaSuccess) return NEO_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_elem_error, &zero, sizeof(zero)) != cudaSuccess) return NEO_ERR_CUDA;
+    *word = h;
+    return NEO_OK;
+}
+
+neo_status elementwise_set_timeout(uint64_t ns) {
+    unsigned long long v = ns;
+    return cudaMemcpyToSymbol(g_elem_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? NEO_OK : NEO_ERR_CUDA;
+}
+
+}  // namespace neo
+
 // ===========================================================================
 // C ABI
 // ===========================================================================
@@ -317,24 +407,50 @@ extern "C" neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype, int64_
     if (S == 0 || Hq + Hkv == 0) return NEO_OK;
     if (!indexes) return NEO_ERR_INVALID_ARG;
 
-    // theta^(-2i/d) per pair, computed in double and rounded once to fp32.
+    // theta^(-2i/d) per pair in double, split as hi (11 significant bits) + lo.
     RopeFreqs fr;
-    for (int i = 0; i < 32; ++i) fr.f[i] = (float)std::pow((double)theta_t, -2.0 * i / 64.0);
+    auto put = [&fr](int at, double f) {
+        int e;
+        const double m = std::frexp(f, &e);                       // f = m * 2^e, m in [0.5, 1)
+        const double hi = std::ldexp(std::floor(m * 2048.0) / 2048.0, e);
+        fr.hi[at] = (float)hi;
+        fr.lo[at] = (float)(f - hi);
+    };
+    for (int i = 0; i < 32; ++i) put(i, std::pow((double)theta_t, -2.0 * i / 64.0));
     for (int i = 0; i < 16; ++i) {
-        const float f = (float)std::pow((double)theta_hw, -2.0 * i / 32.0);
-        fr.f[32 + i] = f;
-        fr.f[48 + i] = f;
+        const double f = std::pow((double)theta_hw, -2.0 * i / 32.0);
+        put(32 + i, f);
+        put(48 + i, f);
     }
-    const int64_t blocks = (S + kTokensPerCta - 1) / kTokensPerCta;
-    if (blocks > 0x7fffffffLL) return NEO_ERR_INVALID_ARG;
+    const int64_t n_items =
+        S * ((Hq + kHeadsPerItem - 1) / kHeadsPerItem + (Hkv + kHeadsPerItem - 1) / kHeadsPerItem);
+    if (n_items >= (int64_t)1 << 31) return NEO_ERR_UNSUPPORTED;
+    const int lpr = dtype == NEO_BF16 ? 8 : 16;   // lanes per row
+    const int64_t items_per_cta = kNormThreads / lpr;
+    const int64_t blocks =
+        std::min<int64_t>((n_items + items_per_cta - 1) / items_per_cta, (int64_t)sm_count() * kNormCtasPerSm);
+    // Ring of kNormDepth slots per warp, each holding one item per row group of the warp.
+    const size_t ring = (size_t)(kNormThreads / 32) * kNormDepth * kHeadsPerItem * 128 * 32 / lpr *
+                        (dtype == NEO_BF16 ? 2 : 4);
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        const int bytes = 96 * 1024;
+        attr_err = cudaFuncSetAttribute(qknorm_rope3_kernel<__nv_bfloat16>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(qknorm_rope3_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            bytes);
+    });
+    if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
     if (dtype == NEO_BF16) {
-        qknorm_rope3_kernel<__nv_bfloat16><<<(unsigned)blocks, kNormThreads, 0, stream>>>(
-            static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), S, Hq, Hkv, indexes,
-            q_norm_w, q_norm_hw_w, k_norm_w, k_norm_hw_w, fr, eps);
+        qknorm_rope3_kernel<__nv_bfloat16><<<(unsigned)blocks, kNormThreads, ring, stream>>>(
+            static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), S, Hq, Hkv, indexes, q_norm_w,
+            q_norm_hw_w, k_norm_w, k_norm_hw_w, fr, eps, n_items);
     } else {
-        qknorm_rope3_kernel<float><<<(unsigned)blocks, kNormThreads, 0, stream>>>(
-            static_cast<float*>(q), static_cast<float*>(k), S, Hq, Hkv, indexes, q_norm_w,
-            q_norm_hw_w, k_norm_w, k_norm_hw_w, fr, eps);
+        qknorm_rope3_kernel<float><<<(unsigned)blocks, kNormThreads, ring, stream>>>(
+            static_cast<float*>(q), static_cast<float*>(k), S, Hq, Hkv, indexes, q_norm_w, q_norm_hw_w,
+            k_norm_w, k_norm_hw_w, fr, eps, n_items);
     }
     return neo::launch_status();
 }

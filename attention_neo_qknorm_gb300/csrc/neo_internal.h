@@ -19,4 +19,8 @@ inline neo_status launch_status() {
 neo_status attention_error_read_clear(cudaStream_t stream, uint32_t* word);
 neo_status attention_set_timeout(uint64_t ns);
 
+// Elementwise translation unit: its own device error word and wait limit.
+neo_status elementwise_error_read_clear(uint32_t* word);
+neo_status elementwise_set_timeout(uint64_t ns);
+
 }  // namespace neo

@@ -6,24 +6,34 @@
 // keys/values of its own sequence followed by the image tokens' own
 // keys/values; query head h reads KV head h / (Hq/Hkv).
 //
-// Kernel shape (one CTA per 128-row query tile; D = 128):
+// Kernel shape (one CTA per 128-row query tile; D = 128; 12 warps):
 //   * A query tile packs the G = Hq/Hkv heads of one KV group for 128/G
 //     consecutive tokens (row r = token * G + head-in-group), so each K/V tile
 //     brought into shared memory serves the whole GQA group.
-//   * Warp 0 (one lane) streams Q once and K/V tiles of 128 keys through a
-//     two-stage TMA ring (128-byte swizzle): first the ceil(L_b/128) tiles of
-//     the packed prefix, then the image tiles. Keys past a segment's end are
-//     masked, so ragged prefixes need no padding.
-//   * Warp 1 (one lane) issues tcgen05.mma: S = Q K^T (A, B K-major in smem,
-//     fp32 accumulator in TMEM, double-buffered so S_{j+1} overlaps the
-//     softmax of tile j) and O += P V (P bf16 read from TMEM, V MN-major in
-//     smem, O accumulated in TMEM).
-//   * Warps 4..7 (one thread per query row = TMEM lane) run the online
-//     softmax in fp32 with exp2 on the SFU, store P to TMEM, rescale O only
-//     when the running maximum grew by more than 2^8 (the final division uses
-//     the same stale maximum, so the result is unchanged), and finally write
-//     O / l as bf16 through shared memory and a TMA store.
-// TMEM: S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,512).
+//   * Warp 0 (one lane) loads Q once and streams K tiles of 128 keys through
+//     a three-stage TMA ring; warp 2 (one lane) streams the V tiles through a
+//     three-stage ring (128-byte swizzle). Prefix tiles come first (from the
+//     packed prefix, ceil(L_b/128) of them), then the image tiles; keys past a
+//     segment's end are masked, so ragged prefixes need no padding.
+//   * Once Q has landed, the softmax warps copy it into TMEM (bf16, one row
+//     per lane), so that both products read their A operand from TMEM and only
+//     K or V from shared memory, which halves the shared-memory traffic of
+//     S = Q K^T.
+//   * Warp 1 (one lane) issues the tcgen05.mma batches of S = Q K^T (Q from
+//     TMEM, K K-major in shared memory, fp32 accumulator in TMEM,
+//     double-buffered so S_{j+1} overlaps the softmax of tile j); warp 3 (one
+//     lane) those of O += P V (P bf16 from TMEM, V MN-major in shared memory,
+//     O accumulated in TMEM).
+//   * Warps 4..11 run the online softmax in fp32. Query row r is TMEM lane r;
+//     warps 4..7 own its key columns [0,64) and warps 8..11 columns [64,128)
+//     (the same TMEM lanes, two warps per sub-partition). The two halves of a
+//     row exchange only their partial maximum through shared memory; each
+//     keeps its own partial row sum until the end. exp2 runs on the SFU, P
+//     goes to TMEM as bf16, and O is rescaled only when the running maximum
+//     grew by more than 2^8 (the final division uses the same stale maximum,
+//     so the result is unchanged). Each half finally writes its 64-wide half
+//     of O / l as bf16 through shared memory and a TMA store.
+// TMEM: Q [0,64) S0 [64,192) S1 [192,320) P [320,384) O [384,512).
 
 #include <cmath>
 #include <cstdint>
@@ -44,29 +54,38 @@ namespace {
 __device__ unsigned int g_dev_error = 0;
 __device__ unsigned long long g_wait_limit_ns = 1000000000ull;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kCluster = 2;                  // CTAs per cluster sharing each K/V tile
+constexpr uint16_t kClusterMask = (1u << kCluster) - 1u;
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kStages = 2;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
 constexpr uint32_t kHalfTile = 128u * 64u * 2u;   // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kTile = 2u * kHalfTile;         // 128 rows x 128 bf16
 
 constexpr uint32_t kSmQ = 0;
 constexpr uint32_t kSmK = kSmQ + kTile;
-constexpr uint32_t kSmV = kSmK + kStages * kTile;
-constexpr uint32_t kSmBar = kSmV + kStages * kTile;
+constexpr uint32_t kSmV = kSmK + kKStages * kTile;
+// Row-max exchange, float [2 tile parity][2 halves][128 rows]. It lives in the Q
+// tile's shared memory, which is free once Q has been copied into TMEM (every
+// softmax thread finishes its copy before S_0 can be issued).
+constexpr uint32_t kSmMax = kSmQ;
+constexpr uint32_t kSmLsum = kSmV + kVStages * kTile;  // float [2 halves][128 rows]
+constexpr uint32_t kSmBar = kSmLsum + 2 * 128 * 4;
 
 enum : int {
     BAR_Q_FULL = 0,
     BAR_K_FULL = 1,
-    BAR_K_EMPTY = BAR_K_FULL + kStages,
-    BAR_V_FULL = BAR_K_EMPTY + kStages,
-    BAR_V_EMPTY = BAR_V_FULL + kStages,
-    BAR_S_FULL = BAR_V_EMPTY + kStages,
+    BAR_K_EMPTY = BAR_K_FULL + kKStages,
+    BAR_V_FULL = BAR_K_EMPTY + kKStages,
+    BAR_V_EMPTY = BAR_V_FULL + kVStages,
+    BAR_S_FULL = BAR_V_EMPTY + kVStages,
     BAR_S_FREE = BAR_S_FULL + 2,
     BAR_P_FULL = BAR_S_FREE + 2,
     BAR_PV_DONE = BAR_P_FULL + 2,
-    BAR_DRAIN = BAR_PV_DONE + 2,
+    BAR_QT_READY = BAR_PV_DONE + 2,   // Q copied into TMEM by the softmax warps
+    BAR_DRAIN = BAR_QT_READY + 1,
     NUM_BARS = BAR_DRAIN + 1
 };
 
@@ -75,8 +94,10 @@ constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
 constexpr uint32_t kSmEpiSkip = kSmAbort + 4;   // written only by the softmax warps
 constexpr uint32_t kSmUsed = kSmEpiSkip + 4;
 constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 
-constexpr uint32_t kTmS0 = 0, kTmP0 = 256, kTmO = 384, kTmCols = 512;
+constexpr uint32_t kTmQ = 0, kTmS0 = 64, kTmP = 320, kTmO = 384, kTmCols = 512;
+constexpr int kSoftmaxThreads = 256;               // warps 4..11
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);   // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, 128, 0, 1);      // V is MN-major
@@ -93,7 +114,7 @@ struct AttnParams {
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, int i) { return sbase + kSmBar + 8u * i; }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                      const __grid_constant__ CUtensorMap tm_kimg,
                      const __grid_constant__ CUtensorMap tm_vimg,
@@ -120,15 +141,20 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int n0 = qt * p.tok_per_tile;
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmAbort);
+    volatile int* epi_skip = reinterpret_cast<volatile int*>(smem + kSmEpiSkip);
     const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
 
-    volatile int* epi_skip = reinterpret_cast<volatile int*>(smem + kSmEpiSkip);
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         *epi_skip = 0;
         for (int i = 0; i < NUM_BARS; ++i) {
             uint32_t count = 1;
-            if (i == BAR_S_FREE || i == BAR_S_FREE + 1 || i == BAR_P_FULL || i == BAR_P_FULL + 1) count = 128;
+            if (i == BAR_S_FREE || i == BAR_S_FREE + 1 || i == BAR_P_FULL || i == BAR_P_FULL + 1 ||
+                i == BAR_QT_READY)
+                count = kSoftmaxThreads;
+            if ((i >= BAR_K_EMPTY && i < BAR_K_EMPTY + kKStages) || (i >= BAR_V_EMPTY && i < BAR_V_EMPTY + kVStages))
+                count = kCluster;                // released by the MMA of every CTA of the cluster
+            if (i == BAR_DRAIN) count = 2;      // one commit from each MMA issuer
             mbar_init(bar_addr(sb, i), count);
         }
         fence_barrier_init();
@@ -139,187 +165,216 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
+    // No CTA may multicast into a peer before the peer's barriers exist.
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
+    const uint32_t crank = cluster_ctarank();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers: K (warp 0) and V (warp 2)
         if (lane == 0) {
-            const uint32_t sQ = sb + kSmQ;
-            mbar_arrive_expect_tx(bar_addr(sb, BAR_Q_FULL), kTile);
-            tma_load_4d(sQ, &tm_q, bar_addr(sb, BAR_Q_FULL), 0, kvh * p.G, n0, b);
-            tma_load_4d(sQ + kHalfTile, &tm_q, bar_addr(sb, BAR_Q_FULL), 64, kvh * p.G, n0, b);
-            int k_issued = 0, v_issued = 0;
+            const bool is_k = warp == 0;
+            if (is_k) {
+                const uint32_t sQ = sb + kSmQ;
+                mbar_arrive_expect_tx(bar_addr(sb, BAR_Q_FULL), kTile);
+                tma_load_4d(sQ, &tm_q, bar_addr(sb, BAR_Q_FULL), 0, kvh * p.G, n0, b);
+                tma_load_4d(sQ + kHalfTile, &tm_q, bar_addr(sb, BAR_Q_FULL), 64, kvh * p.G, n0, b);
+            }
+            const int stages = is_k ? kKStages : kVStages;
+            const int full0 = is_k ? BAR_K_FULL : BAR_V_FULL;
+            const int empty0 = is_k ? BAR_K_EMPTY : BAR_V_EMPTY;
+            const uint32_t ring = sb + (is_k ? kSmK : kSmV);
+            const CUtensorMap* pre_map = is_k ? &tm_kpre : &tm_vpre;
+            const CUtensorMap* img_map = is_k ? &tm_kimg : &tm_vimg;
+            int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % kStages;
-                const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-                const uint32_t sK = sb + kSmK + st * kTile;
-                const uint32_t sV = sb + kSmV + st * kTile;
-                if (!wait(bar_addr(sb, BAR_K_EMPTY + st), ph ^ 1u)) break;
-                const uint32_t kf = bar_addr(sb, BAR_K_FULL + st);
-                mbar_arrive_expect_tx(kf, kTile);
+                const int st = j % stages;
+                const uint32_t ph = (uint32_t)(j / stages) & 1u;
+                if (!wait(bar_addr(sb, empty0 + st), ph ^ 1u)) break;
+                const uint32_t fb = bar_addr(sb, full0 + st);
+                const uint32_t dst = ring + (uint32_t)st * kTile;
+                // The tile's two 64-wide head-dim halves come from the two CTAs of
+                // the cluster, each multicast into both; every CTA expects the full tile.
+                mbar_arrive_expect_tx(fb, kTile);
+                const uint32_t hdst = dst + crank * kHalfTile;
+                const int d0 = 64 * (int)crank;
                 if (j < n_pre) {
-                    const int row = lo + j * kBlockN;
-                    tma_load_3d(sK, &tm_kpre, kf, 0, kvh, row);
-                    tma_load_3d(sK + kHalfTile, &tm_kpre, kf, 64, kvh, row);
+                    tma_load_3d_mc(hdst, pre_map, fb, d0, kvh, lo + j * kBlockN, kClusterMask);
                 } else {
-                    const int row = (j - n_pre) * kBlockN;
-                    tma_load_4d(sK, &tm_kimg, kf, 0, kvh, row, b);
-                    tma_load_4d(sK + kHalfTile, &tm_kimg, kf, 64, kvh, row, b);
+                    tma_load_4d_mc(hdst, img_map, fb, d0, kvh, (j - n_pre) * kBlockN, b, kClusterMask);
                 }
-                k_issued = j + 1;
-                if (!wait(bar_addr(sb, BAR_V_EMPTY + st), ph ^ 1u)) break;
-                const uint32_t vf = bar_addr(sb, BAR_V_FULL + st);
-                mbar_arrive_expect_tx(vf, kTile);
-                if (j < n_pre) {
-                    const int row = lo + j * kBlockN;
-                    tma_load_3d(sV, &tm_vpre, vf, 0, kvh, row);
-                    tma_load_3d(sV + kHalfTile, &tm_vpre, vf, 64, kvh, row);
-                } else {
-                    const int row = (j - n_pre) * kBlockN;
-                    tma_load_4d(sV, &tm_vimg, vf, 0, kvh, row, b);
-                    tma_load_4d(sV + kHalfTile, &tm_vimg, vf, 64, kvh, row, b);
-                }
-                v_issued = j + 1;
+                issued = j + 1;
             }
             if (*abort_flag) {
                 // Let copies already in flight land before the CTA's shared memory goes away.
-                wait(bar_addr(sb, BAR_Q_FULL), 0, false);
-                for (int j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
-                    wait(bar_addr(sb, BAR_K_FULL + j % kStages), (uint32_t)(j / kStages) & 1u, false);
-                for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
-                    wait(bar_addr(sb, BAR_V_FULL + j % kStages), (uint32_t)(j / kStages) & 1u, false);
+                if (is_k) wait(bar_addr(sb, BAR_Q_FULL), 0, false);
+                for (int j = (issued > stages ? issued - stages : 0); j < issued; ++j)
+                    wait(bar_addr(sb, full0 + j % stages), (uint32_t)(j / stages) & 1u, false);
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues S = Q K^T, warp 3 issues O += P V. Issuing a batch blocks
+        // while the tensor pipe's queue is full, so a single issuing thread would
+        // leave the pipe idle whenever it waits on a barrier or commits; two
+        // independent issuers keep it fed. They write disjoint TMEM (S buffers vs
+        // O) and each commits only the barriers of its own product.
         if (lane == 0) {
-            const uint32_t sQ = sb + kSmQ;
-            bool ok = wait(bar_addr(sb, BAR_Q_FULL), 0);
-            tc_fence_after();
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % kStages;
-                if (!wait(bar_addr(sb, BAR_K_FULL + st), (uint32_t)(j / kStages) & 1u)) return false;
-                if (!wait(bar_addr(sb, BAR_S_FREE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u)) return false;
+            bool ok = true;
+            if (warp == 1) {
+                ok = wait(bar_addr(sb, BAR_QT_READY), 0);
                 tc_fence_after();
-                const uint32_t sK = sb + kSmK + st * kTile;
-                const uint32_t d = tmem + kTmS0 + (uint32_t)(j & 1) * 128u;
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const int st = j % kKStages;
+                    if (!wait(bar_addr(sb, BAR_K_FULL + st), (uint32_t)(j / kKStages) & 1u)) break;
+                    if (!wait(bar_addr(sb, BAR_S_FREE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u)) break;
+                    tc_fence_after();
+                    const uint32_t sK = sb + kSmK + (uint32_t)st * kTile;
+                    const uint32_t d = tmem + kTmS0 + (uint32_t)(j & 1) * 128u;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
-                           kIdescS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // 16 head dims per step: 8 TMEM columns of Q, 32 bytes into a K row.
+                        const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                        mma_ts(d, tmem + kTmQ + (uint32_t)kk * 8u, smem_desc_sw128(sK + off, 16, 1024), kIdescS,
+                               kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_addr(sb, BAR_S_FULL + (j & 1)));
+                    mma_commit_mc(bar_addr(sb, BAR_K_EMPTY + st), kClusterMask);
                 }
-                mma_commit(bar_addr(sb, BAR_S_FULL + (j & 1)));
-                mma_commit(bar_addr(sb, BAR_K_EMPTY + st));
-                return true;
-            };
-            auto issue_pv = [&](int j) -> bool {
-                const int st = j % kStages;
-                if (!wait(bar_addr(sb, BAR_P_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u)) return false;
-                if (!wait(bar_addr(sb, BAR_V_FULL + st), (uint32_t)(j / kStages) & 1u)) return false;
-                tc_fence_after();
-                const uint32_t sV = sb + kSmV + st * kTile;
-                const uint32_t pcol = tmem + kTmP0 + (uint32_t)(j & 1) * 64u;
+            } else {
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int st = j % kVStages;
+                    if (!wait(bar_addr(sb, BAR_P_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u)) break;
+                    if (!wait(bar_addr(sb, BAR_V_FULL + st), (uint32_t)(j / kVStages) & 1u)) break;
+                    tc_fence_after();
+                    const uint32_t sV = sb + kSmV + (uint32_t)st * kTile;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // 16 keys per step: rows 16*kk.. of V (2048 bytes); the two
-                    // 64-wide halves of the head dim are 16 KB apart.
-                    mma_ts(tmem + kTmO, pcol + (uint32_t)kk * 8u,
-                           smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // 16 keys per step: rows 16*kk.. of V (2048 bytes); the two
+                        // 64-wide halves of the head dim are 16 KB apart.
+                        mma_ts(tmem + kTmO, tmem + kTmP + (uint32_t)kk * 8u,
+                               smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar_addr(sb, BAR_PV_DONE + (j & 1)));
+                    mma_commit_mc(bar_addr(sb, BAR_V_EMPTY + st), kClusterMask);
                 }
-                mma_commit(bar_addr(sb, BAR_PV_DONE + (j & 1)));
-                mma_commit(bar_addr(sb, BAR_V_EMPTY + st));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-                if (!issue_pv(j)) break;
             }
-            // Drain: every MMA issued above completes before TMEM is released.
+            // Drain: every MMA issued above completes before TMEM is released
+            // (the barrier counts one commit from each issuer).
             mma_commit(bar_addr(sb, BAR_DRAIN));
             wait(bar_addr(sb, BAR_DRAIN), 0, false);
         }
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax + epilogue
+        const int half = (warp - 4) >> 2;          // key columns [64*half, 64*half + 64)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
+        const uint32_t pair_bar = 2u + (uint32_t)quad;   // the two warps sharing these TMEM lanes
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        float* mx_s = reinterpret_cast<float*>(smem + kSmMax);
+        float* ls_s = reinterpret_cast<float*>(smem + kSmLsum);
         float m_used = -INFINITY;
-        float l_sum = 0.f;
-        bool ok = true;
+        float l_part = 0.f;
+        bool failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_Q_FULL), 0));
+        if (!failed) {
+            // Row `row`, head dims [64*half, 64*half + 64): eight 16-byte chunks of
+            // the 128-byte-swizzled Q tile -> 32 TMEM columns (two bf16 per column).
+            const uint8_t* qrow = smem + kSmQ + (uint32_t)half * kHalfTile + (uint32_t)row * 128u;
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
+                r[4 * c + 0] = v.x;
+                r[4 * c + 1] = v.y;
+                r[4 * c + 2] = v.z;
+                r[4 * c + 3] = v.w;
+            }
+            tmem_st32(lane_base + kTmQ + (uint32_t)half * 32u, r);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(bar_addr(sb, BAR_QT_READY));
+        // A failed (timed-out or aborted) wait sets `failed`. The loop then keeps
+        // running without touching TMEM or the pipeline barriers, so that the
+        // two warps of a row pair still meet at every pair barrier.
         for (int j = 0; j < n_tiles; ++j) {
-            ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u));
-            if (!ok) break;
-            tc_fence_after();
-            float s[128];
-            {
-                uint32_t r[128];
-                tmem_ld128(lane_base + kTmS0 + (uint32_t)(j & 1) * 128u, r);
+            bool ok = !failed && __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u));
+            float s[64];
+            float pmax = -INFINITY;
+            const int tile_valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
+            const int valid = tile_valid - half * 64;        // may be <= 0: this half is all padding
+            const bool partial = valid < 64;
+            float* mx_tile = mx_s + (j & 1) * 256;
+            if (ok) {
+                tc_fence_after();
+                {
+                    uint32_t r[64];
+                    tmem_ld64(lane_base + kTmS0 + (uint32_t)(j & 1) * 128u + (uint32_t)half * 64u, r);
 #pragma unroll
-                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+                }
+                tc_fence_before();
+                mbar_arrive(bar_addr(sb, BAR_S_FREE + (j & 1)));
+                // Keys past the end of the prefix or image segment do not exist.
+                if (partial) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                }
+                // Partial row maximum of the raw logits (three-input max tree).
+                float t1[22];
+#pragma unroll
+                for (int i = 0; i < 21; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+                t1[21] = s[63];
+                float t2[8];
+#pragma unroll
+                for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+                t2[7] = t1[21];
+                pmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
+                mx_tile[half * 128 + row] = pmax;
             }
-            tc_fence_before();
-            mbar_arrive(bar_addr(sb, BAR_S_FREE + (j & 1)));
+            // The other half's maximum comes through shared memory; both warps
+            // of the pair leave this barrier with the same verdict.
+            ok = named_barrier_and(pair_bar, 64, ok);
+            failed = !ok;
+            if (failed) continue;
+            const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
 
-            // Keys past the end of the prefix or image segment do not exist.
-            const int valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
-            const bool partial = valid < kBlockN;
-            if (partial) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) s[c] = c < valid ? s[c] : -INFINITY;
-            }
-            // Row maximum of the raw logits: a three-input max tree (depth 5).
-            float mraw;
-            {
-                float t1[43];
-#pragma unroll
-                for (int i = 0; i < 42; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-                t1[42] = fmaxf(s[126], s[127]);
-                float t2[15];
-#pragma unroll
-                for (int i = 0; i < 14; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
-                t2[14] = t1[42];
-                float t3[5];
-#pragma unroll
-                for (int i = 0; i < 5; ++i) t3[i] = fmax3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
-                mraw = fmax3(fmax3(t3[0], t3[1], t3[2]), t3[3], t3[4]);
-            }
             const float m_new = fmaxf(m_used, mraw * p.scale_log2);
             const bool need = m_new > m_used + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ex2(m_used - m_new) : 1.0f;
                 if (need) m_used = m_new;
-                l_sum *= alpha;
+                l_part *= alpha;
                 if (j > 0) {
-                    ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + ((j - 1) & 1)),
-                                                      (uint32_t)((j - 1) >> 1) & 1u));
-                    if (!ok) break;
+                    failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + ((j - 1) & 1)),
+                                                           (uint32_t)((j - 1) >> 1) & 1u));
+                    if (failed) continue;
                     tc_fence_after();
                     uint32_t r[32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld32(lane_base + kTmO + c * 32u, r);
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t ocol = lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u;
+                        tmem_ld32(ocol, r);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(lane_base + kTmO + c * 32u, r);
+                        tmem_st32(ocol, r);
                     }
                     tmem_st_wait();
                 }
             }
             // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU,
-            // eight independent partial sums.
+            // four independent pair accumulators for the row sum.
             const float2 cc = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm = make_float2(-m_used, -m_used);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
-            uint32_t pk[64];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
                 if (partial) {
                     a.x = 2 * c < valid ? a.x : -INFINITY;
@@ -329,77 +384,71 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 acc[c & 3] = fadd2(acc[c & 3], e);
                 pk[c] = pack_bf16x2(e.x, e.y);
             }
-            l_sum += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-            if (j >= 2) {
-                // P buffer j&1 was last read by PV_{j-2}.
-                ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u));
-                if (!ok) break;
+            l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+            if (j >= 1) {
+                // The single P buffer was last read by PV_{j-1}.
+                failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + ((j - 1) & 1)),
+                                                       (uint32_t)((j - 1) >> 1) & 1u));
+                if (failed) continue;
                 tc_fence_after();
             }
-            {
-                const uint32_t pcol = lane_base + kTmP0 + (uint32_t)(j & 1) * 64u;
-                uint32_t r[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = pk[i];
-                tmem_st32(pcol, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = pk[32 + i];
-                tmem_st32(pcol + 32u, r);
-                tmem_st_wait();
-            }
+            tmem_st32(lane_base + kTmP + (uint32_t)half * 32u, pk);
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_addr(sb, BAR_P_FULL + (j & 1)));
         }
+        bool ok = !failed;
 
-        // Only these four warps write epi_skip, and only before this barrier,
+        // Only these eight warps write epi_skip, and only before this barrier,
         // so after it every warp of the group takes the same branch.
         if (ok) {
             const int jl = n_tiles - 1;
             ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (jl & 1)), (uint32_t)(jl >> 1) & 1u));
         }
         if (!ok) *epi_skip = 1;
-        named_barrier_sync(1, 128);
+        ls_s[half * 128 + row] = l_part;
+        named_barrier_sync(1, kSoftmaxThreads);
         if (!*epi_skip) {
-            {
-                tc_fence_after();
-                const float inv_l = 1.0f / l_sum;
-                uint8_t* stage = smem + kSmQ;    // Q is no longer read once the last S is done
+            tc_fence_after();
+            const float l_sum = ls_s[row] + ls_s[128 + row];
+            const float inv_l = 1.0f / l_sum;
+            uint8_t* stage = smem + kSmQ + (uint32_t)half * kHalfTile;   // Q is no longer read
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_base + kTmO + c * 32u, r);
-                    const int half = c >> 1;
+            for (int c = 0; c < 2; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u, r);
 #pragma unroll
-                    for (int qd = 0; qd < 4; ++qd) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[qd * 8 + 0]) * inv_l, __uint_as_float(r[qd * 8 + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(r[qd * 8 + 2]) * inv_l, __uint_as_float(r[qd * 8 + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(r[qd * 8 + 4]) * inv_l, __uint_as_float(r[qd * 8 + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(r[qd * 8 + 6]) * inv_l, __uint_as_float(r[qd * 8 + 7]) * inv_l);
-                        const int chunk = (c & 1) * 4 + qd;
-                        const uint32_t off = (uint32_t)half * kHalfTile + (uint32_t)row * 128u +
-                                             (uint32_t)((chunk ^ (row & 7)) << 4);
-                        *reinterpret_cast<uint4*>(stage + off) = v;
-                    }
+                for (int qd = 0; qd < 4; ++qd) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(r[qd * 8 + 0]) * inv_l, __uint_as_float(r[qd * 8 + 1]) * inv_l);
+                    v.y = pack_bf16x2(__uint_as_float(r[qd * 8 + 2]) * inv_l, __uint_as_float(r[qd * 8 + 3]) * inv_l);
+                    v.z = pack_bf16x2(__uint_as_float(r[qd * 8 + 4]) * inv_l, __uint_as_float(r[qd * 8 + 5]) * inv_l);
+                    v.w = pack_bf16x2(__uint_as_float(r[qd * 8 + 6]) * inv_l, __uint_as_float(r[qd * 8 + 7]) * inv_l);
+                    const int chunk = c * 4 + qd;
+                    const uint32_t off = (uint32_t)row * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
+                    *reinterpret_cast<uint4*>(stage + off) = v;
                 }
-                fence_proxy_async_smem();
-                named_barrier_sync(1, 128);
-                if (row == 0) {
-                    tma_store_4d(&tm_o, sb + kSmQ, 0, kvh * p.G, n0, b);
-                    tma_store_4d(&tm_o, sb + kSmQ + kHalfTile, 64, kvh * p.G, n0, b);
-                    tma_store_commit_and_wait_read();
-                }
-                const int n = n0 + row / p.G;
-                if (p.lse != nullptr && n < p.N) {
-                    const int h = kvh * p.G + row % p.G;
-                    p.lse[((int64_t)b * p.Hq + h) * p.N + n] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
-                }
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(1, kSoftmaxThreads);
+            if (threadIdx.x == 4 * 32 && n0 < p.N) {
+                tma_store_4d(&tm_o, sb + kSmQ, 0, kvh * p.G, n0, b);
+                tma_store_4d(&tm_o, sb + kSmQ + kHalfTile, 64, kvh * p.G, n0, b);
+                tma_store_commit_and_wait_read();
+            }
+            const int n = n0 + row / p.G;
+            if (half == 0 && p.lse != nullptr && n < p.N) {
+                const int h = kvh * p.G + row % p.G;
+                p.lse[((int64_t)b * p.Hq + h) * p.N + n] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    // The peer may still multicast into this CTA's shared memory or arrive on its
+    // barriers until it is done as well.
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmCols);
@@ -537,7 +586,10 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     prm.max_prefix = max_prefix;
     prm.scale_log2 = scale * 1.4426950408889634f;
 
-    const dim3 grid((unsigned)((N + tok_per_tile - 1) / tok_per_tile), (unsigned)Hkv, (unsigned)B);
+    // Query tiles come in clusters of kCluster (a tile past the last token loads,
+    // computes and stores nothing of its own but still shares the K/V stream).
+    const int qtiles = (N + tok_per_tile - 1) / tok_per_tile;
+    const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
     gen_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
     return neo::launch_status();
 }

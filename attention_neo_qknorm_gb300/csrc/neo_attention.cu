@@ -6,34 +6,37 @@
 // keys/values of its own sequence followed by the image tokens' own
 // keys/values; query head h reads KV head h / (Hq/Hkv).
 //
-// Kernel shape (one CTA per 128-row query tile; D = 128; 12 warps):
+// Kernel shape (one CTA per 128-row query tile; D = 128; 12 warps; clusters
+// of two CTAs):
 //   * A query tile packs the G = Hq/Hkv heads of one KV group for 128/G
 //     consecutive tokens (row r = token * G + head-in-group), so each K/V tile
 //     brought into shared memory serves the whole GQA group.
 //   * Warp 0 (one lane) loads Q once and streams K tiles of 128 keys through
 //     a three-stage TMA ring; warp 2 (one lane) streams the V tiles through a
-//     three-stage ring (128-byte swizzle). Prefix tiles come first (from the
-//     packed prefix, ceil(L_b/128) of them), then the image tiles; keys past a
-//     segment's end are masked, so ragged prefixes need no padding.
-//   * Once Q has landed, the softmax warps copy it into TMEM (bf16, one row
-//     per lane), so that both products read their A operand from TMEM and only
-//     K or V from shared memory, which halves the shared-memory traffic of
-//     S = Q K^T.
-//   * Warp 1 (one lane) issues the tcgen05.mma batches of S = Q K^T (Q from
-//     TMEM, K K-major in shared memory, fp32 accumulator in TMEM,
-//     double-buffered so S_{j+1} overlaps the softmax of tile j); warp 3 (one
-//     lane) those of O += P V (P bf16 from TMEM, V MN-major in shared memory,
-//     O accumulated in TMEM).
+//     two-stage ring (128-byte swizzle). The two CTAs of a cluster work on
+//     neighbouring query tiles of the same sequence and KV head: each fetches
+//     one 64-wide head-dim half of every K/V tile and multicasts it into both.
+//     Prefix tiles come first (from the packed prefix, ceil(L_b/128) of
+//     them), then the image tiles; keys past a segment's end are masked, so
+//     ragged prefixes need no padding.
+//   * Warp 1 (one lane) issues the tcgen05.mma batches of S = Q K^T (Q and K
+//     K-major in shared memory, fp32 accumulator in TMEM, three buffers);
+//     warp 3 (one lane) those of O += P V (P bf16 from TMEM, V MN-major in
+//     shared memory, O accumulated in TMEM). Issuing a batch blocks while the
+//     tensor pipe's queue is full, so two independent issuers keep it fed
+//     while either one waits on a barrier.
 //   * Warps 4..11 run the online softmax in fp32. Query row r is TMEM lane r;
 //     warps 4..7 own its key columns [0,64) and warps 8..11 columns [64,128)
 //     (the same TMEM lanes, two warps per sub-partition). The two halves of a
 //     row exchange only their partial maximum through shared memory; each
-//     keeps its own partial row sum until the end. exp2 runs on the SFU, P
-//     goes to TMEM as bf16, and O is rescaled only when the running maximum
+//     keeps its own partial row sum until the end. exp2 runs on the SFU; P_j
+//     goes to TMEM as bf16 over the first 64 columns of the S buffer it came
+//     from, so S_j reuses a buffer only once PV_{j-3} has read it and the
+//     softmax never waits for PV. O is rescaled only when the running maximum
 //     grew by more than 2^8 (the final division uses the same stale maximum,
 //     so the result is unchanged). Each half finally writes its 64-wide half
 //     of O / l as bf16 through shared memory and a TMA store.
-// TMEM: Q [0,64) S0 [64,192) S1 [192,320) P [320,384) O [384,512).
+// TMEM: S0 [0,128) S1 [128,256) S2 [256,384) O [384,512).
 
 #include <cmath>
 #include <cstdint>
@@ -60,18 +63,16 @@ constexpr uint16_t kClusterMask = (1u << kCluster) - 1u;
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kKStages = 3;
-constexpr int kVStages = 3;
+constexpr int kVStages = 2;
+constexpr int kSBufs = 3;                   // S (and P, written over S) buffers in TMEM
 constexpr uint32_t kHalfTile = 128u * 64u * 2u;   // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kTile = 2u * kHalfTile;         // 128 rows x 128 bf16
 
 constexpr uint32_t kSmQ = 0;
 constexpr uint32_t kSmK = kSmQ + kTile;
 constexpr uint32_t kSmV = kSmK + kKStages * kTile;
-// Row-max exchange, float [2 tile parity][2 halves][128 rows]. It lives in the Q
-// tile's shared memory, which is free once Q has been copied into TMEM (every
-// softmax thread finishes its copy before S_0 can be issued).
-constexpr uint32_t kSmMax = kSmQ;
-constexpr uint32_t kSmLsum = kSmV + kVStages * kTile;  // float [2 halves][128 rows]
+constexpr uint32_t kSmMax = kSmV + kVStages * kTile;   // float [2 tile parity][2 halves][128 rows]
+constexpr uint32_t kSmLsum = kSmMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]
 constexpr uint32_t kSmBar = kSmLsum + 2 * 128 * 4;
 
 enum : int {
@@ -81,11 +82,9 @@ enum : int {
     BAR_V_FULL = BAR_K_EMPTY + kKStages,
     BAR_V_EMPTY = BAR_V_FULL + kVStages,
     BAR_S_FULL = BAR_V_EMPTY + kVStages,
-    BAR_S_FREE = BAR_S_FULL + 2,
-    BAR_P_FULL = BAR_S_FREE + 2,
-    BAR_PV_DONE = BAR_P_FULL + 2,
-    BAR_QT_READY = BAR_PV_DONE + 2,   // Q copied into TMEM by the softmax warps
-    BAR_DRAIN = BAR_QT_READY + 1,
+    BAR_P_FULL = BAR_S_FULL + kSBufs,
+    BAR_PV_DONE = BAR_P_FULL + kSBufs,
+    BAR_DRAIN = BAR_PV_DONE + kSBufs,
     NUM_BARS = BAR_DRAIN + 1
 };
 
@@ -96,13 +95,14 @@ constexpr uint32_t kSmUsed = kSmEpiSkip + 4;
 constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 
-constexpr uint32_t kTmQ = 0, kTmS0 = 64, kTmP = 320, kTmO = 384, kTmCols = 512;
+constexpr uint32_t kTmS0 = 0, kTmO = kSBufs * 128, kTmCols = 512;
 constexpr int kSoftmaxThreads = 256;               // warps 4..11
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);   // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, 128, 0, 1);      // V is MN-major
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int kPolyPairs = 0;               // of every 8 exp2 pairs, evaluated on the FMA pipe
 
 struct AttnParams {
     const int32_t* cu_prefix;
@@ -149,8 +149,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         *epi_skip = 0;
         for (int i = 0; i < NUM_BARS; ++i) {
             uint32_t count = 1;
-            if (i == BAR_S_FREE || i == BAR_S_FREE + 1 || i == BAR_P_FULL || i == BAR_P_FULL + 1 ||
-                i == BAR_QT_READY)
+            if (i >= BAR_P_FULL && i < BAR_P_FULL + kSBufs)
                 count = kSoftmaxThreads;
             if ((i >= BAR_K_EMPTY && i < BAR_K_EMPTY + kKStages) || (i >= BAR_V_EMPTY && i < BAR_V_EMPTY + kVStages))
                 count = kCluster;                // released by the MMA of every CTA of the cluster
@@ -224,29 +223,34 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (lane == 0) {
             bool ok = true;
             if (warp == 1) {
-                ok = wait(bar_addr(sb, BAR_QT_READY), 0);
+                const uint32_t sQ = sb + kSmQ;
+                ok = wait(bar_addr(sb, BAR_Q_FULL), 0);
                 tc_fence_after();
                 for (int j = 0; ok && j < n_tiles; ++j) {
                     const int st = j % kKStages;
                     if (!wait(bar_addr(sb, BAR_K_FULL + st), (uint32_t)(j / kKStages) & 1u)) break;
-                    if (!wait(bar_addr(sb, BAR_S_FREE + (j & 1)), ((uint32_t)(j >> 1) & 1u) ^ 1u)) break;
+                    // S buffer j%3 holds P_{j-3} until PV_{j-3} has read it.
+                    const int sbuf = j % kSBufs;
+                    const uint32_t sph = (uint32_t)(j / kSBufs) & 1u;
+                    if (j >= kSBufs && !wait(bar_addr(sb, BAR_PV_DONE + sbuf), sph ^ 1u)) break;
                     tc_fence_after();
                     const uint32_t sK = sb + kSmK + (uint32_t)st * kTile;
-                    const uint32_t d = tmem + kTmS0 + (uint32_t)(j & 1) * 128u;
+                    const uint32_t d = tmem + kTmS0 + (uint32_t)sbuf * 128u;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        // 16 head dims per step: 8 TMEM columns of Q, 32 bytes into a K row.
+                        // 16 head dims per step: 32 bytes into a Q row and a K row.
                         const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-                        mma_ts(d, tmem + kTmQ + (uint32_t)kk * 8u, smem_desc_sw128(sK + off, 16, 1024), kIdescS,
+                        mma_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), kIdescS,
                                kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar_addr(sb, BAR_S_FULL + (j & 1)));
+                    mma_commit(bar_addr(sb, BAR_S_FULL + sbuf));
                     mma_commit_mc(bar_addr(sb, BAR_K_EMPTY + st), kClusterMask);
                 }
             } else {
                 for (int j = 0; j < n_tiles; ++j) {
                     const int st = j % kVStages;
-                    if (!wait(bar_addr(sb, BAR_P_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u)) break;
+                    const int sbuf = j % kSBufs;
+                    if (!wait(bar_addr(sb, BAR_P_FULL + sbuf), (uint32_t)(j / kSBufs) & 1u)) break;
                     if (!wait(bar_addr(sb, BAR_V_FULL + st), (uint32_t)(j / kVStages) & 1u)) break;
                     tc_fence_after();
                     const uint32_t sV = sb + kSmV + (uint32_t)st * kTile;
@@ -254,11 +258,11 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     for (int kk = 0; kk < 8; ++kk) {
                         // 16 keys per step: rows 16*kk.. of V (2048 bytes); the two
                         // 64-wide halves of the head dim are 16 KB apart.
-                        mma_ts(tmem + kTmO, tmem + kTmP + (uint32_t)kk * 8u,
+                        mma_ts(tmem + kTmO, tmem + kTmS0 + (uint32_t)sbuf * 128u + (uint32_t)kk * 8u,
                                smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(bar_addr(sb, BAR_PV_DONE + (j & 1)));
+                    mma_commit(bar_addr(sb, BAR_PV_DONE + sbuf));
                     mma_commit_mc(bar_addr(sb, BAR_V_EMPTY + st), kClusterMask);
                 }
             }
@@ -279,30 +283,14 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         float* ls_s = reinterpret_cast<float*>(smem + kSmLsum);
         float m_used = -INFINITY;
         float l_part = 0.f;
-        bool failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_Q_FULL), 0));
-        if (!failed) {
-            // Row `row`, head dims [64*half, 64*half + 64): eight 16-byte chunks of
-            // the 128-byte-swizzled Q tile -> 32 TMEM columns (two bf16 per column).
-            const uint8_t* qrow = smem + kSmQ + (uint32_t)half * kHalfTile + (uint32_t)row * 128u;
-            uint32_t r[32];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
-                r[4 * c + 0] = v.x;
-                r[4 * c + 1] = v.y;
-                r[4 * c + 2] = v.z;
-                r[4 * c + 3] = v.w;
-            }
-            tmem_st32(lane_base + kTmQ + (uint32_t)half * 32u, r);
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(bar_addr(sb, BAR_QT_READY));
+        bool failed = false;
         // A failed (timed-out or aborted) wait sets `failed`. The loop then keeps
         // running without touching TMEM or the pipeline barriers, so that the
         // two warps of a row pair still meet at every pair barrier.
         for (int j = 0; j < n_tiles; ++j) {
-            bool ok = !failed && __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u));
+            const int sbuf = j % kSBufs;
+            const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
+            bool ok = !failed && __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + sbuf), (uint32_t)(j / kSBufs) & 1u));
             float s[64];
             float pmax = -INFINITY;
             const int tile_valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
@@ -313,12 +301,10 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tc_fence_after();
                 {
                     uint32_t r[64];
-                    tmem_ld64(lane_base + kTmS0 + (uint32_t)(j & 1) * 128u + (uint32_t)half * 64u, r);
+                    tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
 #pragma unroll
                     for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
                 }
-                tc_fence_before();
-                mbar_arrive(bar_addr(sb, BAR_S_FREE + (j & 1)));
                 // Keys past the end of the prefix or image segment do not exist.
                 if (partial) {
 #pragma unroll
@@ -338,9 +324,13 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             // The other half's maximum comes through shared memory; both warps
             // of the pair leave this barrier with the same verdict.
+            // Both halves have read all of S_j into registers once they pass this
+            // barrier, so either may then overwrite it with its part of P_j.
+            tc_fence_before();
             ok = named_barrier_and(pair_bar, 64, ok);
             failed = !ok;
             if (failed) continue;
+            tc_fence_after();
             const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
 
             const float m_new = fmaxf(m_used, mraw * p.scale_log2);
@@ -350,8 +340,8 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 if (need) m_used = m_new;
                 l_part *= alpha;
                 if (j > 0) {
-                    failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + ((j - 1) & 1)),
-                                                           (uint32_t)((j - 1) >> 1) & 1u));
+                    failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (j - 1) % kSBufs),
+                                                           (uint32_t)((j - 1) / kSBufs) & 1u));
                     if (failed) continue;
                     tc_fence_after();
                     uint32_t r[32];
@@ -366,8 +356,9 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     tmem_st_wait();
                 }
             }
-            // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU,
-            // four independent pair accumulators for the row sum.
+            // p = 2^(s*scale*log2e - m): one packed FMA per pair; kPolyPairs of every
+            // 8 pairs take 2^x on the FMA pipe (exp2_poly), the rest on the SFU,
+            // which alone would bound the tile; four pair accumulators for the sum.
             const float2 cc = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm = make_float2(-m_used, -m_used);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -380,22 +371,15 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     a.x = 2 * c < valid ? a.x : -INFINITY;
                     a.y = 2 * c + 1 < valid ? a.y : -INFINITY;
                 }
-                const float2 e = make_float2(ex2(a.x), ex2(a.y));
+                const float2 e = (c & 7) < kPolyPairs ? exp2_poly(a) : make_float2(ex2(a.x), ex2(a.y));
                 acc[c & 3] = fadd2(acc[c & 3], e);
                 pk[c] = pack_bf16x2(e.x, e.y);
             }
             l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-            if (j >= 1) {
-                // The single P buffer was last read by PV_{j-1}.
-                failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + ((j - 1) & 1)),
-                                                       (uint32_t)((j - 1) >> 1) & 1u));
-                if (failed) continue;
-                tc_fence_after();
-            }
-            tmem_st32(lane_base + kTmP + (uint32_t)half * 32u, pk);
+            tmem_st32(lane_base + scol + (uint32_t)half * 32u, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar_addr(sb, BAR_P_FULL + (j & 1)));
+            mbar_arrive(bar_addr(sb, BAR_P_FULL + sbuf));
         }
         bool ok = !failed;
 
@@ -403,7 +387,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // so after it every warp of the group takes the same branch.
         if (ok) {
             const int jl = n_tiles - 1;
-            ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (jl & 1)), (uint32_t)(jl >> 1) & 1u));
+            ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + jl % kSBufs), (uint32_t)(jl / kSBufs) & 1u));
         }
         if (!ok) *epi_skip = 1;
         ls_s[half * 128 + row] = l_part;

@@ -102,7 +102,6 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);   // Q, K b
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, 128, 0, 1);      // V is MN-major
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kPolyPairs = 0;               // of every 8 exp2 pairs, evaluated on the FMA pipe
 
 struct AttnParams {
     const int32_t* cu_prefix;
@@ -356,9 +355,8 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     tmem_st_wait();
                 }
             }
-            // p = 2^(s*scale*log2e - m): one packed FMA per pair; kPolyPairs of every
-            // 8 pairs take 2^x on the FMA pipe (exp2_poly), the rest on the SFU,
-            // which alone would bound the tile; four pair accumulators for the sum.
+            // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU,
+            // four independent pair accumulators for the row sum.
             const float2 cc = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm = make_float2(-m_used, -m_used);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -371,7 +369,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     a.x = 2 * c < valid ? a.x : -INFINITY;
                     a.y = 2 * c + 1 < valid ? a.y : -INFINITY;
                 }
-                const float2 e = (c & 7) < kPolyPairs ? exp2_poly(a) : make_float2(ex2(a.x), ex2(a.y));
+                const float2 e = make_float2(ex2(a.x), ex2(a.y));
                 acc[c & 3] = fadd2(acc[c & 3], e);
                 pk[c] = pack_bf16x2(e.x, e.y);
             }

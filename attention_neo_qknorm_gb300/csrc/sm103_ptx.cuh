@@ -362,29 +362,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return d;
 }
 
-// 2^x for a pair on the FMA pipe, to relieve the special-function unit.
-// Range reduction: n = round(x) by adding 1.5 * 2^23 (the integer lands in
-// the low mantissa bits), f = x - n in [-1/2, 1/2]; 2^f by a degree-3
-// polynomial whose coefficients are a relative-error minimax fit on that
-// interval (max relative error 7.5e-5 with fp32 Horner evaluation); 2^n is
-// added to the exponent field. x is clamped to -127 first, where the result
-// is below 1.2e-38; x must not exceed 127.
-__device__ __forceinline__ float2 exp2_poly(float2 x) {
-    constexpr float kShift = 12582912.0f;   // 1.5 * 2^23
-    constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f;
-    constexpr float c2 = 0.2426111400127411f, c3 = 0.0551716685295105f;
-    x.x = fmaxf(x.x, -127.0f);
-    x.y = fmaxf(x.y, -127.0f);
-    const float2 t = fadd2(x, make_float2(kShift, kShift));
-    const float2 n = fadd2(t, make_float2(-kShift, -kShift));
-    const float2 f = ffma2(n, make_float2(-1.0f, -1.0f), x);   // x - n, exact
-    float2 p = ffma2(make_float2(c3, c3), f, make_float2(c2, c2));
-    p = ffma2(p, f, make_float2(c1, c1));
-    p = ffma2(p, f, make_float2(c0, c0));
-    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
-}
-
 // 2^x on the special-function unit (ex2.approx.ftz.f32): 2^-inf = +0.
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -339,6 +339,69 @@ flow_euler_kernel(float* __restrict__ z, const float* __restrict__ x0, int64_t n
     }
 }
 
+// ---------------------------------------------------------------------------
+// Classifier-free guidance fused with the Euler step ([U1] §2.7). Every
+// branch's velocity is v_X = (x0_X - z) / den and the guidance weights of a
+// branch sum to one, so the guided velocity is v = (sum_X w_X x0_X - z) / den;
+// the kernel reads the K x0 buffers the branch needs once, with z.
+// ---------------------------------------------------------------------------
+template <int K>
+__global__ void __launch_bounds__(kEulerThreads)
+flow_cfg_kernel(float* __restrict__ z, const float* __restrict__ xa, const float* __restrict__ xb,
+                const float* __restrict__ xc, int64_t n, float wa, float wb, float wc, float den, float dt,
+                float* __restrict__ v_out) {
+    const int64_t n4 = n >> 2;
+    const int64_t stride = (int64_t)gridDim.x * kEulerThreads;
+    const int64_t tid = (int64_t)blockIdx.x * kEulerThreads + threadIdx.x;
+    float4* z4 = reinterpret_cast<float4*>(z);
+    const float4* a4 = reinterpret_cast<const float4*>(xa);
+    const float4* b4 = reinterpret_cast<const float4*>(xb);
+    const float4* c4 = reinterpret_cast<const float4*>(xc);
+    float4* v4 = reinterpret_cast<float4*>(v_out);
+    auto mix = [&](float a, float b, float c) {
+        float x = wa * a;
+        if (K > 1) x = fmaf(wb, b, x);
+        if (K > 2) x = fmaf(wc, c, x);
+        return x;
+    };
+    for (int64_t base = tid; base < n4; base += stride * 2) {
+        float4 zz[2], aa[2], bb[2], cc[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < n4) {
+                zz[u] = z4[i];
+                aa[u] = __ldg(a4 + i);
+                if (K > 1) bb[u] = __ldg(b4 + i);
+                if (K > 2) cc[u] = __ldg(c4 + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < n4) {
+                float4 v;
+                v.x = (mix(aa[u].x, bb[u].x, cc[u].x) - zz[u].x) / den;
+                v.y = (mix(aa[u].y, bb[u].y, cc[u].y) - zz[u].y) / den;
+                v.z = (mix(aa[u].z, bb[u].z, cc[u].z) - zz[u].z) / den;
+                v.w = (mix(aa[u].w, bb[u].w, cc[u].w) - zz[u].w) / den;
+                float4 zn;
+                zn.x = fmaf(dt, v.x, zz[u].x);
+                zn.y = fmaf(dt, v.y, zz[u].y);
+                zn.z = fmaf(dt, v.z, zz[u].z);
+                zn.w = fmaf(dt, v.w, zz[u].w);
+                z4[i] = zn;
+                if (v_out) v4[i] = v;
+            }
+        }
+    }
+    for (int64_t i = (n4 << 2) + tid; i < n; i += stride) {
+        const float v = (mix(xa[i], K > 1 ? xb[i] : 0.f, K > 2 ? xc[i] : 0.f) - z[i]) / den;
+        z[i] = fmaf(dt, v, z[i]);
+        if (v_out) v_out[i] = v;
+    }
+}
+
 }  // namespace
 
 namespace neo {
@@ -470,5 +533,56 @@ extern "C" neo_status neo_flow_euler_step(float* z, const float* x0_hat, int64_t
     const int64_t want = (n4 + kEulerThreads * kEulerUnroll - 1) / (kEulerThreads * kEulerUnroll);
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
     flow_euler_kernel<<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, x0_hat, n, den, dt, v_out);
+    return neo::launch_status();
+}
+
+extern "C" neo_status neo_flow_cfg_euler_step(float* z, const float* x0_cond, const float* x0_text_uncond,
+                                              const float* x0_uncond, int64_t n, float t, float t_next,
+                                              float t_eps, float cfg_scale, float img_cfg_scale,
+                                              float cfg_interval_lo, float cfg_interval_hi, float* v_out,
+                                              int32_t* branch_out, cudaStream_t stream) {
+    if (n < 0 || !std::isfinite(t) || !std::isfinite(t_next) || !std::isfinite(t_eps) ||
+        !std::isfinite(cfg_scale) || !std::isfinite(img_cfg_scale) || !std::isfinite(cfg_interval_lo) ||
+        !std::isfinite(cfg_interval_hi))
+        return NEO_ERR_INVALID_ARG;
+    // Branch of the inference loop ([U1] section 2.7).
+    const bool use_cfg = (t > cfg_interval_lo && t < cfg_interval_hi) || cfg_interval_lo == 0.0f;
+    int branch;
+    if (!use_cfg || (cfg_scale == 1.0f && img_cfg_scale == 1.0f)) branch = NEO_CFG_NONE;
+    else if (img_cfg_scale == 1.0f) branch = NEO_CFG_TEXT;
+    else if (cfg_scale == img_cfg_scale) branch = NEO_CFG_CLASSIC;
+    else branch = NEO_CFG_DUAL;
+    if (branch_out) *branch_out = branch;
+    // Weights on (cond, text-uncond, uncond); each row sums to one.
+    const float* xa = x0_cond;
+    const float* xb = nullptr;
+    const float* xc = nullptr;
+    float wa = 1.f, wb = 0.f, wc = 0.f;
+    int K = 1;
+    if (branch == NEO_CFG_TEXT) {
+        xb = x0_text_uncond; wa = cfg_scale; wb = 1.f - cfg_scale; K = 2;
+    } else if (branch == NEO_CFG_CLASSIC) {
+        xb = x0_uncond; wa = cfg_scale; wb = 1.f - cfg_scale; K = 2;
+    } else if (branch == NEO_CFG_DUAL) {
+        xb = x0_text_uncond; xc = x0_uncond;
+        wa = cfg_scale; wb = img_cfg_scale - cfg_scale; wc = 1.f - img_cfg_scale; K = 3;
+    }
+    if (n == 0) return NEO_OK;
+    if (!z || !xa || (K > 1 && !xb) || (K > 2 && !xc)) return NEO_ERR_INVALID_ARG;
+    if (!neo::aligned16(z) || !neo::aligned16(xa) || (xb && !neo::aligned16(xb)) || (xc && !neo::aligned16(xc)) ||
+        (v_out && !neo::aligned16(v_out)))
+        return NEO_ERR_INVALID_ARG;
+    const float den = std::fmax(1.0f - t, t_eps);
+    if (!(den > 0.f)) return NEO_ERR_INVALID_ARG;
+    const float dt = t_next - t;
+    const int64_t n4 = (n + 3) / 4;
+    const int64_t want = (n4 + kEulerThreads * 2 - 1) / (kEulerThreads * 2);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
+    if (K == 1)
+        flow_cfg_kernel<1><<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, xa, xa, xa, n, wa, wb, wc, den, dt, v_out);
+    else if (K == 2)
+        flow_cfg_kernel<2><<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, xa, xb, xb, n, wa, wb, wc, den, dt, v_out);
+    else
+        flow_cfg_kernel<3><<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, xa, xb, xc, n, wa, wb, wc, den, dt, v_out);
     return neo::launch_status();
 }

@@ -52,10 +52,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended (issuing nothing) for up to
+// `hint_ns` while the phase is incomplete; completion wakes it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // A wait with a wall-clock limit. On expiry it raises the CTA's abort flag
 // and ORs `err_bit` into the device error word; a raised abort flag (set by
 // another role of the same CTA) also ends the wait. Returns false in both
 // cases so that the caller can unwind without touching the pipeline.
+constexpr uint32_t kSleepHintNs = 20000;
+
 struct BoundedWait {
     volatile int* abort_flag;
     unsigned int* err_word;
@@ -67,7 +83,9 @@ struct BoundedWait {
         if (mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(bar, parity)) return true;
+            // Suspended rather than spinning, so that waiting warps leave the
+            // issue slots of their sub-partition to the softmax warps.
+            if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
             if ((it & 31u) == 0) {
                 if (honour_abort && *abort_flag) return false;
                 if (globaltimer_ns() - t0 > limit_ns || it > (1u << 30)) {

@@ -22,8 +22,10 @@ NEO_BF16, NEO_F32 = 0, 1
 NEO_MASK_FULL, NEO_MASK_BLOCK_CAUSAL = 0, 1
 NEO_SEG_TEXT, NEO_SEG_IMAGE = 0, 1
 NEO_DEVERR_TIMEOUT, NEO_DEVERR_BAD_PREFIX = 0x1, 0x2
+NEO_CFG_NONE, NEO_CFG_TEXT, NEO_CFG_CLASSIC, NEO_CFG_DUAL = range(4)
 
 EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
+           "neo_flow_cfg_euler_step",
            "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version")
 
 
@@ -57,13 +59,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.neo_gen_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, c_int, _vp, _i64, _i32, c_int, c_int, c_int,
                                       c_int, c_int, c_int, _vp, _vp, _f32, _vp, _vp, _vp]
     lib.neo_flow_euler_step.argtypes = [_vp, _vp, _i64, _f32, _f32, _f32, _vp, _vp]
+    lib.neo_flow_cfg_euler_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _f32, _f32, _f32, _f32, _f32, _f32, _f32,
+                                            _vp, ctypes.POINTER(ctypes.c_int32), _vp]
     lib.neo_status_string.argtypes = [c_int]
     lib.neo_status_string.restype = ctypes.c_char_p
     lib.neo_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.neo_set_wait_timeout_ns.argtypes = [_u64]
     lib.neo_version.argtypes = []
     for name in ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
-                 "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version"):
+                 "neo_flow_cfg_euler_step", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -171,6 +175,23 @@ def neo_flow_euler_step(z, x0_hat, t, t_next, t_eps=0.02, v_out=None, stream=Non
     _check(load_library().neo_flow_euler_step(
         _ptr(z, torch.float32, "z"), _ptr(x0_hat, torch.float32, "x0_hat"), n, float(t), float(t_next),
         float(t_eps), _ptr(v_out, torch.float32, "v_out"), _stream(stream, z)), "neo_flow_euler_step")
+
+
+def neo_flow_cfg_euler_step(z, x0_cond, x0_text_uncond, x0_uncond, t, t_next, cfg_scale, img_cfg_scale,
+                            cfg_interval=(0.0, 1.0), t_eps=0.02, v_out=None, stream=None) -> int:
+    """In place: classifier-free-guided Euler step; returns the branch taken."""
+    n = z.numel()
+    for x in (x0_cond, x0_text_uncond, x0_uncond, v_out):
+        if x is not None and x.numel() != n:
+            raise ValueError("all buffers must have the same number of elements")
+    branch = ctypes.c_int32(-1)
+    _check(load_library().neo_flow_cfg_euler_step(
+        _ptr(z, torch.float32, "z"), _ptr(x0_cond, torch.float32, "x0_cond"),
+        _ptr(x0_text_uncond, torch.float32, "x0_text_uncond"), _ptr(x0_uncond, torch.float32, "x0_uncond"), n,
+        float(t), float(t_next), float(t_eps), float(cfg_scale), float(img_cfg_scale), float(cfg_interval[0]),
+        float(cfg_interval[1]), _ptr(v_out, torch.float32, "v_out"), ctypes.byref(branch), _stream(stream, z)),
+        "neo_flow_cfg_euler_step")
+    return branch.value
 
 
 def neo_get_device_error(stream=None) -> tuple[int, int]:

@@ -158,6 +158,37 @@ neo_status neo_flow_euler_step(float* z, const float* x0_hat, int64_t n,
                                float t, float t_next, float t_eps,
                                float* v_out, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Classifier-free guidance fused with the Euler step.
+ * [U1] section 2.7 (three-branch CFG of the inference loop): with the
+ * conditional (c), text-unconditional (tu: images kept, text removed) and
+ * unconditional (u) predictions, per-branch velocities
+ * v_X = (x0_X - z) / max(1 - t, t_eps) and g = cfg_scale, g_img = img_cfg_scale:
+ *   use_cfg = (lo < t < hi) || lo == 0        (cfg_interval = [lo, hi])
+ *   NEO_CFG_NONE    (!use_cfg or g == g_img == 1): v = v_c
+ *   NEO_CFG_TEXT    (g_img == 1):                  v = v_tu + g (v_c - v_tu)
+ *   NEO_CFG_CLASSIC (g == g_img):                  v = v_u + g (v_c - v_u)
+ *   NEO_CFG_DUAL    (otherwise):                   v = v_u + g (v_c - v_tu) + g_img (v_tu - v_u)
+ * then z = z + (t_next - t) v. The branch is chosen on the host; only the
+ * predictions it needs are read (the others may be NULL).
+ *
+ * z: fp32 [n] in place; x0_*: fp32 [n]; v_out: optional fp32 [n];
+ * branch_out: optional HOST int32 receiving the branch taken.
+ * Returns NEO_ERR_INVALID_ARG if a prediction the branch needs is NULL.
+ * ------------------------------------------------------------------------ */
+#define NEO_CFG_NONE 0
+#define NEO_CFG_TEXT 1
+#define NEO_CFG_CLASSIC 2
+#define NEO_CFG_DUAL 3
+
+neo_status neo_flow_cfg_euler_step(float* z, const float* x0_cond,
+                                   const float* x0_text_uncond,
+                                   const float* x0_uncond, int64_t n, float t,
+                                   float t_next, float t_eps, float cfg_scale,
+                                   float img_cfg_scale, float cfg_interval_lo,
+                                   float cfg_interval_hi, float* v_out,
+                                   int32_t* branch_out, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* neo_status_string(neo_status s);
 

@@ -6,9 +6,15 @@ its Python binding never import it; the two share no code.
 """
 
 from .neo_oracle import (  # noqa: F401
+    CFG_CLASSIC,
+    CFG_DUAL,
+    CFG_NONE,
+    CFG_TEXT,
     HEAD_DIM,
     MASK_BLOCK_CAUSAL,
     MASK_FULL,
+    cfg_branch,
+    flow_cfg_euler_step,
     flow_euler_step,
     flow_interpolant,
     flow_target_velocity,

@@ -270,3 +270,63 @@ def flow_interpolant(x, noise, t, sigma):
 def flow_target_velocity(x, z_t, t):
     """Training target v* = (x - z_t) / (1 - t) ([U1] §2.2)."""
     return (np.asarray(x, np.float64) - np.asarray(z_t, np.float64)) / (1.0 - t)
+
+
+# ---------------------------------------------------------------------------
+# NEXT: classifier-free guidance fused with the Euler step
+# ---------------------------------------------------------------------------
+CFG_NONE, CFG_TEXT, CFG_CLASSIC, CFG_DUAL = 0, 1, 2, 3
+
+
+def cfg_branch(t, cfg_scale, img_cfg_scale, cfg_interval=(0.0, 1.0)):
+    """Which of the four inference branches of [U1] §2.7 applies at time t.
+
+    use_cfg = (interval[0] < t < interval[1]) or interval[0] == 0;
+    no CFG (or both scales 1) -> 0; img_cfg_scale == 1 -> 1 (text CFG against
+    the text-unconditional branch); cfg_scale == img_cfg_scale -> 2 (classic
+    CFG against the fully unconditional branch); otherwise -> 3 (both).
+    """
+    lo, hi = cfg_interval
+    use_cfg = (lo < t < hi) or lo == 0
+    if not use_cfg or (cfg_scale == 1 and img_cfg_scale == 1):
+        return CFG_NONE
+    if img_cfg_scale == 1:
+        return CFG_TEXT
+    if cfg_scale == img_cfg_scale:
+        return CFG_CLASSIC
+    return CFG_DUAL
+
+
+def flow_cfg_euler_step(z, x0_cond, x0_text_uncond, x0_uncond, t, t_next, cfg_scale, img_cfg_scale,
+                        cfg_interval=(0.0, 1.0), t_eps=0.02):
+    """Guided velocity and Euler step ([U1] §2.7, three-branch CFG; [U15]
+    §Flow matching without a VAE for x0 -> v).
+
+    Each branch's x0 prediction becomes a velocity v_X = (x0_X - z) / max(1 - t,
+    t_eps); the branches combine as
+      0: v = v_c
+      1: v = v_tu + g (v_c - v_tu)
+      2: v = v_u + g (v_c - v_u)
+      3: v = v_u + g (v_c - v_tu) + g_img (v_tu - v_u)
+    with g = cfg_scale, g_img = img_cfg_scale, c = conditional, tu = text
+    unconditional (image kept), u = unconditional; then z += (t_next - t) v.
+    Returns (z_next, v, branch).
+    """
+    z = np.asarray(z, np.float64)
+    den = max(1.0 - float(t), float(t_eps))
+    vel = lambda x0: (np.asarray(x0, np.float64) - z) / den
+    g, gi = float(cfg_scale), float(img_cfg_scale)
+    branch = cfg_branch(float(t), g, gi, cfg_interval)
+    v_c = vel(x0_cond)
+    if branch == CFG_NONE:
+        v = v_c
+    elif branch == CFG_TEXT:
+        v_tu = vel(x0_text_uncond)
+        v = v_tu + g * (v_c - v_tu)
+    elif branch == CFG_CLASSIC:
+        v_u = vel(x0_uncond)
+        v = v_u + g * (v_c - v_u)
+    else:
+        v_tu, v_u = vel(x0_text_uncond), vel(x0_uncond)
+        v = v_u + g * (v_c - v_tu) + gi * (v_tu - v_u)
+    return z + (float(t_next) - float(t)) * v, v, branch

@@ -117,3 +117,21 @@ def test_positions_rejects_bad_segments(lib):
     assert f(FAKE, 10, segs, 0, None) == neo.NEO_ERR_INVALID_ARG
     bad = (Seg * 1)(Seg(5, 0, 1, 1))
     assert f(FAKE, 1, bad, 1, None) == neo.NEO_ERR_INVALID_ARG
+
+
+def test_cfg_euler_rejects_missing_predictions(lib):
+    f = lib.neo_flow_cfg_euler_step
+    br = ctypes.c_int32(-1)
+    # text CFG needs the text-unconditional prediction
+    assert f(FAKE, FAKE, None, None, 8, 0.5, 0.6, 0.02, 4.0, 1.0, 0.0, 1.0, None, ctypes.byref(br), None) == \
+        neo.NEO_ERR_INVALID_ARG
+    assert br.value == neo.NEO_CFG_TEXT
+    # dual CFG needs both
+    assert f(FAKE, FAKE, FAKE, None, 8, 0.5, 0.6, 0.02, 4.0, 1.5, 0.0, 1.0, None, ctypes.byref(br), None) == \
+        neo.NEO_ERR_INVALID_ARG
+    assert br.value == neo.NEO_CFG_DUAL
+    # n == 0: nothing to do, but the branch is still reported
+    assert f(None, None, None, None, 0, 0.7, 0.8, 0.02, 3.0, 3.0, 0.6, 1.0, None, ctypes.byref(br), None) == neo.NEO_OK
+    assert br.value == neo.NEO_CFG_CLASSIC
+    assert f(FAKE, MISALIGNED, None, None, 8, 0.5, 0.6, 0.02, 1.0, 1.0, 0.0, 1.0, None, None, None) == \
+        neo.NEO_ERR_INVALID_ARG

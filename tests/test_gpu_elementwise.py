@@ -130,3 +130,42 @@ def test_euler_ten_steps_against_oracle(gpu_lib):
         neo.neo_flow_euler_step(zd, xs[k].cuda(), float(t), float(tn), 0.02)
         rz, _ = O.flow_euler_step(rz, f64(xs[k]), t, tn, np.float32(0.02))
     assert rel_frob(f64(zd), rz) <= F32_TOL
+
+
+@pytest.mark.parametrize("g,gi,interval,t", [
+    (1.0, 1.0, (0.0, 1.0), 0.3),     # no guidance
+    (4.0, 1.0, (0.0, 1.0), 0.3),     # text CFG, the T2I default scales
+    (3.0, 3.0, (0.0, 1.0), 0.5),     # classic CFG
+    (4.0, 1.5, (0.0, 1.0), 0.7),     # dual (Eq. 6)
+    (4.0, 1.5, (0.6, 1.0), 0.5),     # outside the interval: unguided
+    (4.0, 1.5, (0.6, 1.0), 0.95),    # inside, clamped by t_eps
+])
+def test_cfg_euler_matches_oracle(gpu_lib, g, gi, interval, t):
+    gen = torch.Generator().manual_seed(50)
+    n = 3 * 4096 + 7
+    z, c, tu, u = (torch.randn(n, generator=gen) for _ in range(4))
+    zd, vd = z.cuda(), torch.empty(n, device="cuda")
+    branch = neo.neo_flow_cfg_euler_step(zd, c.cuda(), tu.cuda(), u.cuda(), t, t + 0.05, g, gi, interval,
+                                         v_out=vd)
+    f32 = np.float32
+    rz, rv, rb = O.flow_cfg_euler_step(f64(z), f64(c), f64(tu), f64(u), f32(t), f32(t + 0.05), f32(g), f32(gi),
+                                       (f32(interval[0]), f32(interval[1])), t_eps=f32(0.02))
+    assert branch == rb
+    for got, ref in ((f64(zd), rz), (f64(vd), rv)):
+        assert rel_frob(got, ref) <= F32_TOL
+        assert max_abs(got, ref) <= F32_TOL * max(1.0, float(np.abs(ref).max()))
+
+
+def test_cfg_euler_reads_only_the_needed_predictions(gpu_lib):
+    """The unguided branch needs no unconditional predictions (None is fine);
+    a guided branch without them is rejected before anything runs."""
+    z = torch.randn(1000, device="cuda")
+    c = torch.randn(1000, device="cuda")
+    ref = z.clone()
+    neo.neo_flow_euler_step(ref, c, 0.4, 0.5)
+    zz = z.clone()
+    assert neo.neo_flow_cfg_euler_step(zz, c, None, None, 0.4, 0.5, 1.0, 1.0) == neo.NEO_CFG_NONE
+    assert torch.equal(zz, ref)
+    with pytest.raises(neo.NeoError) as e:
+        neo.neo_flow_cfg_euler_step(z.clone(), c, None, None, 0.4, 0.5, 4.0, 1.0)
+    assert e.value.status == neo.NEO_ERR_INVALID_ARG

@@ -325,3 +325,60 @@ def test_flow_t_eps_clamp_and_elementwise_permutation():
     a, _ = O.flow_euler_step(z, x, 0.2, 0.3)
     b, _ = O.flow_euler_step(z[perm], x[perm], 0.2, 0.3)
     np.testing.assert_array_equal(a[perm], b)
+
+
+# ---------------------------------------------------------------- CFG + Euler
+def _cfg_inputs(n=64, seed=40):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(n), g.standard_normal(n), g.standard_normal(n), g.standard_normal(n)
+
+
+def test_cfg_branch_selection_follows_the_pages():
+    """Branches of the inference loop: no CFG, text CFG (img scale 1), classic
+    (equal scales), dual; the interval gates CFG unless its start is 0."""
+    assert O.cfg_branch(0.5, 4.0, 1.0) == O.CFG_TEXT          # the T2I default (4.0, 1.0)
+    assert O.cfg_branch(0.5, 1.0, 1.0) == O.CFG_NONE
+    assert O.cfg_branch(0.5, 3.0, 3.0) == O.CFG_CLASSIC
+    assert O.cfg_branch(0.5, 4.0, 1.5) == O.CFG_DUAL
+    assert O.cfg_branch(0.5, 4.0, 1.5, (0.6, 1.0)) == O.CFG_NONE
+    assert O.cfg_branch(0.7, 4.0, 1.5, (0.6, 1.0)) == O.CFG_DUAL
+    assert O.cfg_branch(0.6, 4.0, 1.5, (0.6, 1.0)) == O.CFG_NONE    # strict bounds
+    assert O.cfg_branch(0.95, 4.0, 1.5, (0.0, 0.5)) == O.CFG_DUAL    # start 0: always on
+
+
+def test_cfg_none_is_the_plain_euler_step():
+    z, c, tu, u = _cfg_inputs()
+    zc, vc, br = O.flow_cfg_euler_step(z, c, tu, u, 0.3, 0.4, 1.0, 1.0)
+    ze, ve = O.flow_euler_step(z, c, 0.3, 0.4)
+    assert br == O.CFG_NONE
+    np.testing.assert_array_equal(zc, ze)
+    np.testing.assert_array_equal(vc, ve)
+
+
+def test_cfg_text_branch_is_an_affine_blend():
+    """The page notes the text-CFG branch equals (1 - g) * v_tu + g * v_c."""
+    z, c, tu, u = _cfg_inputs(seed=41)
+    t, g = 0.45, 4.0
+    _, v, _ = O.flow_cfg_euler_step(z, c, tu, u, t, t + 0.1, g, 1.0)
+    _, vc = O.flow_euler_step(z, c, t, t + 0.1)
+    _, vtu = O.flow_euler_step(z, tu, t, t + 0.1)
+    np.testing.assert_allclose(v, (1 - g) * vtu + g * vc, rtol=1e-12, atol=1e-12)
+
+
+def test_cfg_dual_reduces_to_the_two_scale_branches():
+    """Eq. 6 with img scale 1 is the text branch; with equal scales it is the
+    classic branch; guidance weights sum to one, so a common x0 gives the
+    unguided step."""
+    z, c, tu, u = _cfg_inputs(seed=42)
+    t = 0.2
+    den = 1 - t
+    vc, vtu, vu = (c - z) / den, (tu - z) / den, (u - z) / den
+    dual = lambda g, gi: vu + g * (vc - vtu) + gi * (vtu - vu)
+    np.testing.assert_allclose(dual(3.0, 1.0), vtu + 3.0 * (vc - vtu), rtol=1e-12)
+    np.testing.assert_allclose(dual(2.5, 2.5), vu + 2.5 * (vc - vu), rtol=1e-12)
+    _, v, br = O.flow_cfg_euler_step(z, c, tu, u, t, t + 0.1, 3.0, 1.7)
+    assert br == O.CFG_DUAL
+    np.testing.assert_allclose(v, dual(3.0, 1.7), rtol=1e-12, atol=1e-12)
+    zs, _, _ = O.flow_cfg_euler_step(z, c, c, c, t, t + 0.1, 3.0, 1.7)
+    ze, _ = O.flow_euler_step(z, c, t, t + 0.1)
+    np.testing.assert_allclose(zs, ze, rtol=1e-12, atol=1e-12)

@@ -1,5 +1,6 @@
 // Status strings, the device error word and the wait limit of libneo.
 
+#include <cmath>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -37,3 +38,31 @@ extern "C" neo_status neo_set_wait_timeout_ns(uint64_t ns) {
 }
 
 extern "C" int neo_version(void) { return 100; }
+
+extern "C" neo_status neo_time_schedule(float* t_out, int n_steps, float shift) {
+    if (!t_out || n_steps < 1 || !(shift > 0.f) || !std::isfinite(shift)) return NEO_ERR_INVALID_ARG;
+    const double s = shift;
+    for (int k = 0; k <= n_steps; ++k) {
+        const double t = (double)k / n_steps;
+        double sigma = 1.0 - t;
+        sigma = s * sigma / (1.0 + (s - 1.0) * sigma);
+        t_out[k] = (float)(1.0 - sigma);
+    }
+    return NEO_OK;
+}
+
+extern "C" neo_status neo_noise_scale(int grid_h, int grid_w, int merge, float base_seq_len, float base_scale,
+                                      int mode, float max_value, float* out) {
+    if (!out || grid_h < 1 || grid_w < 1 || merge < 1 || !(base_seq_len > 0.f) || !std::isfinite(base_scale) ||
+        !std::isfinite(max_value))
+        return NEO_ERR_INVALID_ARG;
+    double s = base_scale;
+    if (mode == NEO_NOISE_RESOLUTION || mode == NEO_NOISE_DYNAMIC || mode == NEO_NOISE_DYNAMIC_SQRT) {
+        s = std::sqrt((double)grid_h * grid_w / ((double)merge * merge) / base_seq_len) * base_scale;
+        if (mode == NEO_NOISE_DYNAMIC_SQRT) s = std::sqrt(s);
+    } else if (mode != NEO_NOISE_CONSTANT) {
+        return NEO_ERR_INVALID_ARG;
+    }
+    *out = (float)std::fmin(s, (double)max_value);
+    return NEO_OK;
+}

@@ -402,6 +402,103 @@ flow_cfg_kernel(float* __restrict__ z, const float* __restrict__ xa, const float
     }
 }
 
+// z_0 = sigma * eps ([U1] §2.3).
+__global__ void __launch_bounds__(kEulerThreads)
+scale_noise_kernel(float* z, const float* eps, int64_t n, float sigma) {
+    const int64_t n4 = n >> 2;
+    const int64_t stride = (int64_t)gridDim.x * kEulerThreads;
+    const int64_t tid = (int64_t)blockIdx.x * kEulerThreads + threadIdx.x;
+    for (int64_t i = tid; i < n4; i += stride) {
+        float4 e = reinterpret_cast<const float4*>(eps)[i];
+        e.x *= sigma; e.y *= sigma; e.z *= sigma; e.w *= sigma;
+        reinterpret_cast<float4*>(z)[i] = e;
+    }
+    for (int64_t i = (n4 << 2) + tid; i < n; i += stride) z[i] = sigma * eps[i];
+}
+
+// ---------------------------------------------------------------------------
+// Interleaved 2-D RoPE of the vision tower ([U15] §Vision tower): channels
+// [0, C/2) turn with the patch column, [C/2, C) with the patch row, pairs
+// (2i, 2i+1) share the angle pos * theta^(-2i/(C/2)). A thread owns four
+// consecutive channels (two pairs) of a patch; consecutive threads cover
+// consecutive channels, so every access is coalesced.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Quad;   // four consecutive channels
+
+template <>
+struct Quad<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[4]) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&y)[4]) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(y[2], y[3]);
+        *reinterpret_cast<uint2*>(p) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+};
+
+template <>
+struct Quad<float> {
+    static __device__ __forceinline__ void load(const float* p, float (&x)[4]) {
+        const float4 u = *reinterpret_cast<const float4*>(p);
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float (&y)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+rope2d_interleaved_kernel(T* __restrict__ x, int64_t n_tokens, int rows, int cols, int C, float log2_theta) {
+    // Thread (tx, block b): channel quads tx, tx + blockDim.x, ... of patches
+    // b, b + gridDim.x, ...; the quad's two frequencies are computed once.
+    const int quads = C / 4;
+    const int d = C / 2;
+    const int per_img = rows * cols;
+    for (int q = threadIdx.x; q < quads; q += blockDim.x) {
+        const int ch = q * 4;
+        const bool row_half = ch >= d;
+        const int i0 = (ch - (row_half ? d : 0)) >> 1;
+        float fh[2], fl[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            fh[k] = exp2f(-2.0f * (float)(i0 + k) / (float)d * log2_theta);
+            fl[k] = 0.f;    // positions are patch indices: pos * f needs no extra precision
+        }
+        constexpr int U = 4;   // patches in flight per thread
+        for (int64_t tb = blockIdx.x; tb < n_tokens; tb += (int64_t)gridDim.x * U) {
+            float v[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t tok = tb + (int64_t)u * gridDim.x;
+                if (tok < n_tokens) Quad<T>::load(x + tok * C + ch, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t tok = tb + (int64_t)u * gridDim.x;
+                if (tok >= n_tokens) continue;
+                const int t = (int)(tok % per_img);
+                const float pos = (float)(row_half ? t / cols : t % cols);
+                float o[4];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float sn, cs;
+                    rope_sincos(pos, fh[k], fl[k], &sn, &cs);
+                    o[2 * k] = fmaf(v[u][2 * k], cs, -v[u][2 * k + 1] * sn);
+                    o[2 * k + 1] = fmaf(v[u][2 * k + 1], cs, v[u][2 * k] * sn);
+                }
+                Quad<T>::store(x + tok * C + ch, o);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 namespace neo {
@@ -584,5 +681,37 @@ extern "C" neo_status neo_flow_cfg_euler_step(float* z, const float* x0_cond, co
         flow_cfg_kernel<2><<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, xa, xb, xb, n, wa, wb, wc, den, dt, v_out);
     else
         flow_cfg_kernel<3><<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, xa, xb, xc, n, wa, wb, wc, den, dt, v_out);
+    return neo::launch_status();
+}
+
+extern "C" neo_status neo_scale_noise(float* z, const float* eps, int64_t n, float sigma, cudaStream_t stream) {
+    if (n < 0 || !std::isfinite(sigma)) return NEO_ERR_INVALID_ARG;
+    if (n == 0) return NEO_OK;
+    if (!z || !eps || !neo::aligned16(z) || !neo::aligned16(eps)) return NEO_ERR_INVALID_ARG;
+    const int64_t n4 = (n + 3) / 4;
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((n4 + kEulerThreads - 1) / kEulerThreads,
+                                                                  (int64_t)sm_count() * 8));
+    scale_noise_kernel<<<(unsigned)blocks, kEulerThreads, 0, stream>>>(z, eps, n, sigma);
+    return neo::launch_status();
+}
+
+extern "C" neo_status neo_rope2d_interleaved(void* x, neo_dtype dtype, int64_t n_images, int rows, int cols, int C,
+                                             float theta, cudaStream_t stream) {
+    if (n_images < 0 || rows < 0 || cols < 0 || C < 4 || C % 4 != 0 || !(theta > 0.f) || !std::isfinite(theta))
+        return NEO_ERR_INVALID_ARG;
+    if (dtype != NEO_BF16 && dtype != NEO_F32) return NEO_ERR_INVALID_ARG;
+    const int64_t n_tokens = n_images * rows * cols;
+    if (n_tokens == 0) return NEO_OK;
+    if (!x || !neo::aligned16(x) || (dtype == NEO_BF16 && C % 8 != 0)) return NEO_ERR_INVALID_ARG;
+    const float log2_theta = (float)std::log2((double)theta);
+    if ((int64_t)rows * cols > 0x7fffffffLL) return NEO_ERR_UNSUPPORTED;
+    const int threads = std::min(256, C / 4);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(n_tokens, (int64_t)sm_count() * 16));
+    if (dtype == NEO_BF16)
+        rope2d_interleaved_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
+            static_cast<__nv_bfloat16*>(x), n_tokens, rows, cols, C, log2_theta);
+    else
+        rope2d_interleaved_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(static_cast<float*>(x), n_tokens,
+                                                                                    rows, cols, C, log2_theta);
     return neo::launch_status();
 }

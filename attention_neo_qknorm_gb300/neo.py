@@ -23,9 +23,11 @@ NEO_MASK_FULL, NEO_MASK_BLOCK_CAUSAL = 0, 1
 NEO_SEG_TEXT, NEO_SEG_IMAGE = 0, 1
 NEO_DEVERR_TIMEOUT, NEO_DEVERR_BAD_PREFIX = 0x1, 0x2
 NEO_CFG_NONE, NEO_CFG_TEXT, NEO_CFG_CLASSIC, NEO_CFG_DUAL = range(4)
+NEO_NOISE_RESOLUTION, NEO_NOISE_DYNAMIC, NEO_NOISE_DYNAMIC_SQRT, NEO_NOISE_CONSTANT = range(4)
 
 EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
-           "neo_flow_cfg_euler_step",
+           "neo_flow_cfg_euler_step", "neo_time_schedule", "neo_noise_scale", "neo_scale_noise",
+           "neo_rope2d_interleaved",
            "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version")
 
 
@@ -61,13 +63,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.neo_flow_euler_step.argtypes = [_vp, _vp, _i64, _f32, _f32, _f32, _vp, _vp]
     lib.neo_flow_cfg_euler_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _f32, _f32, _f32, _f32, _f32, _f32, _f32,
                                             _vp, ctypes.POINTER(ctypes.c_int32), _vp]
+    lib.neo_time_schedule.argtypes = [_vp, c_int, _f32]
+    lib.neo_noise_scale.argtypes = [c_int, c_int, c_int, _f32, _f32, c_int, _f32, ctypes.POINTER(ctypes.c_float)]
+    lib.neo_scale_noise.argtypes = [_vp, _vp, _i64, _f32, _vp]
+    lib.neo_rope2d_interleaved.argtypes = [_vp, c_int, _i64, c_int, c_int, c_int, _f32, _vp]
     lib.neo_status_string.argtypes = [c_int]
     lib.neo_status_string.restype = ctypes.c_char_p
     lib.neo_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.neo_set_wait_timeout_ns.argtypes = [_u64]
     lib.neo_version.argtypes = []
     for name in ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
-                 "neo_flow_cfg_euler_step", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version"):
+                 "neo_flow_cfg_euler_step", "neo_time_schedule", "neo_noise_scale", "neo_scale_noise",
+           "neo_rope2d_interleaved", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -192,6 +199,42 @@ def neo_flow_cfg_euler_step(z, x0_cond, x0_text_uncond, x0_uncond, t, t_next, cf
         float(cfg_interval[1]), _ptr(v_out, torch.float32, "v_out"), ctypes.byref(branch), _stream(stream, z)),
         "neo_flow_cfg_euler_step")
     return branch.value
+
+
+def neo_time_schedule(n_steps: int, shift: float) -> list:
+    """Host: the shifted time grid, n_steps + 1 floats from 0 to 1."""
+    out = (ctypes.c_float * (n_steps + 1))()
+    _check(load_library().neo_time_schedule(ctypes.cast(out, ctypes.c_void_p), int(n_steps), float(shift)),
+           "neo_time_schedule")
+    return list(out)
+
+
+def neo_noise_scale(grid_h, grid_w, merge=2, base_seq_len=64.0, base_scale=1.0, mode=NEO_NOISE_RESOLUTION,
+                    max_value=16.0) -> float:
+    """Host: the resolution-dependent noise scale sigma_R."""
+    out = ctypes.c_float(0.0)
+    _check(load_library().neo_noise_scale(int(grid_h), int(grid_w), int(merge), float(base_seq_len),
+                                          float(base_scale), int(mode), float(max_value), ctypes.byref(out)),
+           "neo_noise_scale")
+    return out.value
+
+
+def neo_scale_noise(z, eps, sigma, stream=None):
+    """z <- sigma * eps (fp32, same number of elements; z may be eps)."""
+    if z.numel() != eps.numel():
+        raise ValueError("z and eps must have the same number of elements")
+    _check(load_library().neo_scale_noise(_ptr(z, torch.float32, "z"), _ptr(eps, torch.float32, "eps"), z.numel(),
+                                          float(sigma), _stream(stream, z)), "neo_scale_noise")
+
+
+def neo_rope2d_interleaved(x, rows, cols, theta=1e4, stream=None):
+    """In place: x [n_images, rows * cols, C] (bf16 or fp32)."""
+    dt = _DT.get(x.dtype)
+    if dt is None or x.dim() != 3 or x.shape[1] != rows * cols:
+        raise ValueError("x must be [n_images, rows*cols, C] bf16 or fp32")
+    _check(load_library().neo_rope2d_interleaved(_ptr(x, what="x"), dt, x.shape[0], int(rows), int(cols),
+                                                 x.shape[2], float(theta), _stream(stream, x)),
+           "neo_rope2d_interleaved")
 
 
 def neo_get_device_error(stream=None) -> tuple[int, int]:

@@ -189,6 +189,58 @@ neo_status neo_flow_cfg_euler_step(float* z, const float* x0_cond,
                                    float cfg_interval_hi, float* v_out,
                                    int32_t* branch_out, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Sampler pieces around the Euler step.
+ *
+ * neo_time_schedule: HOST computation of the shifted time grid
+ * ([U15] section "Timestep schedule", "standard" branch). t_out (host,
+ * n_steps + 1 floats) receives, for t_k = k / n_steps,
+ *   sigma = 1 - t_k; sigma = shift*sigma / (1 + (shift-1)*sigma); t = 1 - sigma
+ * (computed in double, rounded once). n_steps >= 1, shift > 0.
+ *
+ * neo_noise_scale: HOST computation of the resolution-dependent noise scale
+ * ([U15] section "Timestep and noise-scale conditioning"; [U1] section 2.3):
+ *   NEO_NOISE_RESOLUTION / NEO_NOISE_DYNAMIC:
+ *       s = sqrt(grid_h * grid_w / merge^2 / base_seq_len) * base_scale
+ *   NEO_NOISE_DYNAMIC_SQRT: sqrt of the above;  NEO_NOISE_CONSTANT: base_scale
+ *   result = min(s, max_value) (16.0 in the export code) -> *out (host).
+ * grid_h, grid_w count patches before the merge.
+ *
+ * neo_scale_noise: DEVICE z[i] = sigma * eps[i] for i < n (the initial sample
+ * z_0 = sigma_R * eps; eps is the caller's standard-normal draw). z may alias
+ * eps. fp32, 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+#define NEO_NOISE_RESOLUTION 0
+#define NEO_NOISE_DYNAMIC 1
+#define NEO_NOISE_DYNAMIC_SQRT 2
+#define NEO_NOISE_CONSTANT 3
+
+neo_status neo_time_schedule(float* t_out, int n_steps, float shift);
+
+neo_status neo_noise_scale(int grid_h, int grid_w, int merge, float base_seq_len,
+                           float base_scale, int mode, float max_value,
+                           float* out);
+
+neo_status neo_scale_noise(float* z, const float* eps, int64_t n, float sigma,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Interleaved 2-D rotary embedding of the vision tower, in place.
+ * [U15] section "Vision tower": on the patch features (C = 1024 channels in
+ * the model), channels [0, C/2) turn with the patch's column index and
+ * [C/2, C) with its row index; pairs (2i, 2i+1) share one angle (interleaved,
+ * unlike the backbone's half split), base theta (1e4). Within a half of width
+ * d = C/2, pair i turns by p * theta^(-2i/d):
+ *   (u, w) -> (u cos a - w sin a, w cos a + u sin a).
+ *
+ * x: [n_images, rows * cols, C] of `dtype` (bf16 or fp32), patch
+ * t = r * cols + c of each image; fp32 arithmetic, one rounding at the end.
+ * C must be a multiple of 4 (of 8 for bf16).
+ * ------------------------------------------------------------------------ */
+neo_status neo_rope2d_interleaved(void* x, neo_dtype dtype, int64_t n_images,
+                                  int rows, int cols, int C, float theta,
+                                  cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* neo_status_string(neo_status s);
 

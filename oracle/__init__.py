@@ -13,15 +13,23 @@ from .neo_oracle import (  # noqa: F401
     HEAD_DIM,
     MASK_BLOCK_CAUSAL,
     MASK_FULL,
+    NOISE_CONSTANT,
+    NOISE_DYNAMIC,
+    NOISE_DYNAMIC_SQRT,
+    NOISE_RESOLUTION,
     cfg_branch,
     flow_cfg_euler_step,
     flow_euler_step,
     flow_interpolant,
     flow_target_velocity,
     gen_attention,
+    initial_noise,
+    noise_scale,
     positions,
     qknorm_halves,
     qknorm_rope3,
+    rope2d_interleaved,
     rope3,
     rope_slices,
+    time_schedule,
 )

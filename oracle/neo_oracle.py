@@ -330,3 +330,79 @@ def flow_cfg_euler_step(z, x0_cond, x0_text_uncond, x0_uncond, t, t_next, cfg_sc
         v_tu, v_u = vel(x0_text_uncond), vel(x0_uncond)
         v = v_u + g * (v_c - v_tu) + gi * (v_tu - v_u)
     return z + (float(t_next) - float(t)) * v, v, branch
+
+
+# ---------------------------------------------------------------------------
+# NEXT: sampler pieces (time grid, resolution-dependent noise scale)
+# ---------------------------------------------------------------------------
+def time_schedule(n_steps, shift):
+    """Shifted time grid of the sampler ([U15] §Timestep schedule, "standard"
+    branch): every point of the uniform grid t_k = k / n_steps (READING A14:
+    n_steps + 1 points from 0 to 1) is mapped by
+        sigma = 1 - t;  sigma = shift * sigma / (1 + (shift - 1) * sigma);  t = 1 - sigma.
+    """
+    out = []
+    for k in range(n_steps + 1):
+        t = k / n_steps
+        sigma = 1.0 - t
+        sigma = shift * sigma / (1.0 + (shift - 1.0) * sigma)
+        out.append(1.0 - sigma)
+    return np.asarray(out, np.float64)
+
+
+NOISE_RESOLUTION, NOISE_DYNAMIC, NOISE_DYNAMIC_SQRT, NOISE_CONSTANT = 0, 1, 2, 3
+
+
+def noise_scale(grid_h, grid_w, merge, base_seq_len, base_scale, mode, max_value=16.0):
+    """Resolution-dependent noise scale sigma_R ([U15] §Timestep and
+    noise-scale conditioning; [U1] §2.3): in the resolution / dynamic modes
+    sigma = sqrt(grid_h * grid_w / merge^2 / base_seq_len) * base_scale, the
+    dynamic_sqrt mode takes one more square root of that, the constant mode
+    keeps base_scale; the result is capped at max_value (16.0 in the export
+    code; READING A9: the cap is a parameter). grid_h, grid_w count patches
+    before the merge, so grid_h * grid_w / merge^2 is the token count N."""
+    s = float(base_scale)
+    if mode in (NOISE_RESOLUTION, NOISE_DYNAMIC, NOISE_DYNAMIC_SQRT):
+        s = np.sqrt(grid_h * grid_w / merge ** 2 / float(base_seq_len)) * float(base_scale)
+        if mode == NOISE_DYNAMIC_SQRT:
+            s = np.sqrt(s)
+    return float(min(s, float(max_value)))
+
+
+def initial_noise(eps, sigma):
+    """z_0 = sigma_R * eps ([U1] §2.3: the initial sample is the scaled
+    standard normal draw)."""
+    return float(sigma) * np.asarray(eps, np.float64)
+
+
+# ---------------------------------------------------------------------------
+# NEXT: interleaved 2-D rotary embedding of the vision tower
+# ---------------------------------------------------------------------------
+def rope2d_interleaved(x, rows, cols, theta=1e4):
+    """Interleaved 2-D RoPE of the patch features ([U15] §Vision tower).
+
+    x: [n_images, rows * cols, C] with patch t = r * cols + c. Channels
+    [0, C/2) turn with the patch's column (x) index and [C/2, C) with its row
+    (y) index; the rotation is interleaved: pair (2i, 2i+1) of a half shares
+    one angle. READING A15: within a half of width d = C/2, pair i turns by
+    p * theta^(-2i/d) (the standard RoPE frequencies over that half), with
+        (u, w) -> (u cos a - w sin a, w cos a + u sin a),  (u, w) = (x[2i], x[2i+1]).
+    Returns a new float64 array.
+    """
+    x = np.asarray(x, np.float64)
+    n_img, T, C = x.shape
+    assert T == rows * cols and C % 4 == 0
+    d = C // 2
+    r = np.repeat(np.arange(rows, dtype=np.float64), cols)
+    c = np.tile(np.arange(cols, dtype=np.float64), rows)
+    i = np.arange(d // 2, dtype=np.float64)
+    freq = theta ** (-2.0 * i / d)
+    out = x.copy()
+    for off, pos in ((0, c), (d, r)):
+        a = pos[:, None] * freq[None, :]                    # [T, d/2]
+        cos, sin = np.cos(a)[None], np.sin(a)[None]
+        u = x[:, :, off:off + d:2]
+        w = x[:, :, off + 1:off + d:2]
+        out[:, :, off:off + d:2] = u * cos - w * sin
+        out[:, :, off + 1:off + d:2] = w * cos + u * sin
+    return out

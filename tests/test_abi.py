@@ -135,3 +135,30 @@ def test_cfg_euler_rejects_missing_predictions(lib):
     assert br.value == neo.NEO_CFG_CLASSIC
     assert f(FAKE, MISALIGNED, None, None, 8, 0.5, 0.6, 0.02, 1.0, 1.0, 0.0, 1.0, None, None, None) == \
         neo.NEO_ERR_INVALID_ARG
+
+
+def test_sampler_host_functions_match_the_oracle(lib):
+    """Host-side entry points: no GPU involved."""
+    import numpy as np
+    import oracle as O
+    for n, shift in ((50, 3.0), (10, 1.0), (20, 0.5)):
+        np.testing.assert_allclose(neo.neo_time_schedule(n, shift), O.time_schedule(n, shift), atol=1e-7)
+    for args in ((128, 128, 2, 64, 1.0, 0), (128, 128, 2, 64, 1.0, 2), (64, 64, 2, 64, 3.0, 1), (128, 128, 2, 64, 3.0, 0),
+                 (100, 60, 2, 64, 0.7, 3)):
+        assert neo.neo_noise_scale(*args) == pytest.approx(O.noise_scale(*args), rel=1e-6)
+    assert neo.neo_noise_scale(128, 128, 2, 64, 3.0, 0, max_value=8.0) == pytest.approx(8.0)
+    with pytest.raises(neo.NeoError):
+        neo.neo_time_schedule(0, 3.0)
+    with pytest.raises(neo.NeoError):
+        neo.neo_noise_scale(128, 128, 2, 64, 1.0, 9)
+    assert lib.neo_scale_noise(None, None, 0, 2.0, None) == neo.NEO_OK
+    assert lib.neo_scale_noise(MISALIGNED, FAKE, 8, 2.0, None) == neo.NEO_ERR_INVALID_ARG
+
+
+def test_rope2d_rejects_bad_arguments(lib):
+    f = lib.neo_rope2d_interleaved
+    assert f(FAKE, neo.NEO_BF16, 1, 4, 4, 1022, 1e4, None) == neo.NEO_ERR_INVALID_ARG    # C % 4
+    assert f(FAKE, neo.NEO_BF16, 1, 4, 4, 12, 1e4, None) == neo.NEO_ERR_INVALID_ARG      # bf16 needs C % 8
+    assert f(FAKE, neo.NEO_BF16, 1, 4, 4, 16, -1.0, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(MISALIGNED, neo.NEO_F32, 1, 4, 4, 16, 1e4, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(None, neo.NEO_F32, 0, 4, 4, 16, 1e4, None) == neo.NEO_OK

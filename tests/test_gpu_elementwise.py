@@ -169,3 +169,39 @@ def test_cfg_euler_reads_only_the_needed_predictions(gpu_lib):
     with pytest.raises(neo.NeoError) as e:
         neo.neo_flow_cfg_euler_step(z.clone(), c, None, None, 0.4, 0.5, 4.0, 1.0)
     assert e.value.status == neo.NEO_ERR_INVALID_ARG
+
+
+def test_scale_noise_and_sampler_loop(gpu_lib):
+    """Initial sample z_0 = sigma_R * eps, then the shifted schedule drives ten
+    Euler steps with a fixed x0_hat; compared with the oracle step by step."""
+    gen = torch.Generator().manual_seed(70)
+    n = 4096 * 3 + 3
+    eps, x0 = torch.randn(n, generator=gen), torch.randn(n, generator=gen)
+    sigma = neo.neo_noise_scale(64, 64, 2, 64.0, 1.0)
+    z = torch.empty(n, device="cuda")
+    neo.neo_scale_noise(z, eps.cuda(), sigma)
+    rz = O.initial_noise(f64(eps), np.float32(sigma))
+    assert max_abs(f64(z), rz) <= 6e-8 * float(np.abs(rz).max())   # one fp32 rounding
+    ts = neo.neo_time_schedule(10, 3.0)
+    xd = x0.cuda()
+    for k in range(10):
+        neo.neo_flow_euler_step(z, xd, ts[k], ts[k + 1])
+        rz, _ = O.flow_euler_step(rz, f64(x0), np.float32(ts[k]), np.float32(ts[k + 1]), np.float32(0.02))
+    assert rel_frob(f64(z), rz) <= F32_TOL
+
+
+@pytest.mark.parametrize("dtype,n_img,rows,cols,C", [
+    (torch.bfloat16, 2, 5, 7, 1024),      # model width, ragged grid
+    (torch.bfloat16, 1, 128, 128, 1024),  # the 2048^2 patch grid (before the 2x2 merge)
+    (torch.float32, 3, 4, 6, 64),
+])
+def test_rope2d_interleaved_matches_oracle(gpu_lib, dtype, n_img, rows, cols, C):
+    gen = torch.Generator().manual_seed(rows * cols + C)
+    x = torch.randn(n_img, rows * cols, C, generator=gen).to(dtype)
+    xd = x.cuda()
+    neo.neo_rope2d_interleaved(xd, rows, cols)
+    ref = O.rope2d_interleaved(f64(x), rows, cols)
+    if dtype == torch.bfloat16:
+        assert_bf16_close(f64(xd), ref, "rope2d bf16")
+    else:
+        assert max_abs(f64(xd), ref) < 2e-5

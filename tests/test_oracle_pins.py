@@ -382,3 +382,87 @@ def test_cfg_dual_reduces_to_the_two_scale_branches():
     zs, _, _ = O.flow_cfg_euler_step(z, c, c, c, t, t + 0.1, 3.0, 1.7)
     ze, _ = O.flow_euler_step(z, c, t, t + 0.1)
     np.testing.assert_allclose(zs, ze, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- sampler pieces
+def test_time_schedule_endpoints_identity_and_shift_map():
+    for n in (10, 50):
+        for shift in (1.0, 3.0, 0.5):
+            t = O.time_schedule(n, shift)
+            assert t.shape == (n + 1,)
+            assert t[0] == pytest.approx(0.0, abs=1e-15) and t[-1] == pytest.approx(1.0, abs=1e-15)
+            assert np.all(np.diff(t) > 0)
+    np.testing.assert_allclose(O.time_schedule(50, 1.0), np.linspace(0, 1, 51), atol=1e-15)
+    # shift s maps sigma = 1/2 to s/(1+s): with s = 3 the middle of the grid lands at t = 1/4
+    assert O.time_schedule(10, 3.0)[5] == pytest.approx(0.25, abs=1e-15)
+    # shift > 1 spends more steps at high noise (small t)
+    assert np.all(O.time_schedule(50, 3.0)[1:-1] < np.linspace(0, 1, 51)[1:-1])
+
+
+def test_noise_scale_closed_forms():
+    # 2048^2: 128x128 patches, merge 2 -> 4096 tokens; base 64 tokens -> sqrt(64) = 8
+    assert O.noise_scale(128, 128, 2, 64, 1.0, O.NOISE_RESOLUTION) == pytest.approx(8.0)
+    assert O.noise_scale(128, 128, 2, 64, 1.0, O.NOISE_DYNAMIC) == pytest.approx(8.0)
+    assert O.noise_scale(128, 128, 2, 64, 1.0, O.NOISE_DYNAMIC_SQRT) == pytest.approx(np.sqrt(8.0))
+    assert O.noise_scale(64, 64, 2, 64, 1.0, O.NOISE_RESOLUTION) == pytest.approx(4.0)   # 1024^2
+    assert O.noise_scale(128, 128, 2, 64, 3.0, O.NOISE_RESOLUTION) == pytest.approx(16.0)   # capped
+    assert O.noise_scale(128, 128, 2, 64, 3.0, O.NOISE_RESOLUTION, max_value=8.0) == pytest.approx(8.0)
+    assert O.noise_scale(128, 128, 2, 64, 0.7, O.NOISE_CONSTANT) == pytest.approx(0.7)
+    # sigma grows as the square root of the token count
+    r = O.noise_scale(96, 96, 2, 64, 1.0, O.NOISE_RESOLUTION) / O.noise_scale(48, 48, 2, 64, 1.0, O.NOISE_RESOLUTION)
+    assert r == pytest.approx(2.0)
+
+
+def test_initial_noise_scales_the_draw():
+    e = np.random.default_rng(60).standard_normal(100)
+    np.testing.assert_array_equal(O.initial_noise(e, 1.0), e)
+    np.testing.assert_allclose(O.initial_noise(e, 8.0), 8.0 * e, rtol=1e-15)
+
+
+# ---------------------------------------------------------------- interleaved 2-D RoPE
+def test_rope2d_identity_at_origin_and_pair_norms():
+    g = np.random.default_rng(80)
+    x = g.standard_normal((2, 12, 16))                       # 3 x 4 grid, 16 channels
+    y = O.rope2d_interleaved(x, 3, 4)
+    np.testing.assert_array_equal(y[:, 0], x[:, 0])          # patch (0, 0)
+    n0 = x[..., 0::2] ** 2 + x[..., 1::2] ** 2
+    n1 = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=1e-12)
+
+
+def test_rope2d_halves_follow_column_and_row():
+    g = np.random.default_rng(81)
+    x = np.broadcast_to(g.standard_normal(16), (1, 12, 16)).copy()
+    y = O.rope2d_interleaved(x, 3, 4)
+    # same column (c = 1), different rows: first half equal, second half differs
+    np.testing.assert_allclose(y[0, 1, :8], y[0, 5, :8], rtol=1e-13)
+    assert not np.allclose(y[0, 1, 8:], y[0, 5, 8:])
+    # same row (r = 2), different columns: second half equal
+    np.testing.assert_allclose(y[0, 8, 8:], y[0, 11, 8:], rtol=1e-13)
+    assert not np.allclose(y[0, 8, :8], y[0, 11, :8])
+
+
+def test_rope2d_interleaved_complex_closed_form():
+    """Pair (2i, 2i+1) is the complex number x[2i] + i x[2i+1] times
+    exp(i p f_i) with f_0 = 1 and a geometric ratio theta^(-2/d)."""
+    C, theta = 16, 1e4
+    d = C // 2
+    x = np.zeros((1, 2, C))
+    x[0, 1, 0:d:2] = 1.0                                     # patch (0, 1): column 1
+    y = O.rope2d_interleaved(x, 1, 2, theta)
+    f = np.angle(y[0, 1, 0:d:2] + 1j * y[0, 1, 1:d:2])
+    assert f[0] == pytest.approx(1.0, rel=1e-14)
+    np.testing.assert_allclose(f[1:] / f[:-1], theta ** (-2.0 / d), rtol=1e-12)
+    assert np.all(y[0, 1, d:] == 0)                          # row index 0: second half untouched (zeros)
+
+
+def test_rope2d_relative_position():
+    g = np.random.default_rng(82)
+    q, k = g.standard_normal(32), g.standard_normal(32)
+    rows, cols = 6, 7
+    xq = np.broadcast_to(q, (1, rows * cols, 32)).copy()
+    xk = np.broadcast_to(k, (1, rows * cols, 32)).copy()
+    yq, yk = O.rope2d_interleaved(xq, rows, cols), O.rope2d_interleaved(xk, rows, cols)
+    dot = lambda a, b: float(np.sum(yq[0, a] * yk[0, b]))
+    # (r, c) pairs with equal offsets give equal dot products
+    assert dot(1 * cols + 2, 3 * cols + 5) == pytest.approx(dot(2 * cols + 1, 4 * cols + 4), rel=1e-10)

@@ -4,7 +4,9 @@
 // "Mixture of Transformers" items 1-2 and "GQA fusion does not apply"): every
 // noisy image token's query attends, without a mask, over the frozen prefix
 // keys/values of its own sequence followed by the image tokens' own
-// keys/values; query head h reads KV head h / (Hq/Hkv).
+// keys/values; query head h reads KV head h / (Hq/Hkv). The same kernel also
+// applies the block-causal mask of the mixed prefill (section "Block-causal
+// attention"): key j visible to query i iff T_j == T_i or j <= i.
 //
 // Kernel shape (one CTA per 128-row query tile; D = 128; 12 warps; clusters
 // of two CTAs):
@@ -105,6 +107,9 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 struct AttnParams {
     const int32_t* cu_prefix;
+    const int32_t* t_prefix;   // block-causal mode: temporal index of every packed prefix row
+    const int32_t* t_img;      // block-causal mode: temporal index of every image token [B*N]
+    int mask_mode;
     float* lse;
     int64_t total_prefix;
     int B, N, Hq, Hkv, G, tok_per_tile, max_prefix;
@@ -113,6 +118,7 @@ struct AttnParams {
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, int i) { return sbase + kSmBar + 8u * i; }
 
+template <bool kBlockCausal>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                      const __grid_constant__ CUtensorMap tm_kimg,
@@ -283,6 +289,15 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         float m_used = -INFINITY;
         float l_part = 0.f;
         bool failed = false;
+        // Block-causal mode (section "Block-causal attention"): key j of the
+        // concatenated order [prefix ; image] is visible to query i iff
+        // T_j == T_i or j <= i. This row's query is image token n (clamped for
+        // padding rows, whose output is never stored), i = L + n.
+        constexpr bool block_causal = kBlockCausal;
+        const int n_row = min(n0 + row / p.G, p.N - 1);
+        const int i_row = L + n_row;
+        const int t_row = block_causal ? __ldg(p.t_img + (int64_t)b * p.N + n_row) : 0;
+        const int i_first = L + n0;                         // smallest query index of the tile
         // A failed (timed-out or aborted) wait sets `failed`. The loop then keeps
         // running without touching TMEM or the pipeline barriers, so that the
         // two warps of a row pair still meet at every pair barrier.
@@ -294,7 +309,34 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             float pmax = -INFINITY;
             const int tile_valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
             const int valid = tile_valid - half * 64;        // may be <= 0: this half is all padding
-            const bool partial = valid < 64;
+            // Concatenated index of this thread's first key column.
+            const int key0 = (j < n_pre ? j * kBlockN : L + (j - n_pre) * kBlockN) + half * 64;
+            // A tile entirely at or below the tile's first query needs no block-causal mask.
+            const bool causal_here = block_causal && key0 + 63 > i_first;
+            const bool partial = valid < 64 || causal_here;
+            uint64_t keep = 0;                               // bit c: key column c is visible
+            if constexpr (block_causal) {
+                if (partial) {
+                    for (int c = 0; c < 64; ++c) {
+                        bool vis = c < valid;
+                        if (vis && causal_here) {
+                            const int kj = key0 + c;
+                            if (kj > i_row) {
+                                const int tj = j < n_pre ? __ldg(p.t_prefix + lo + kj)
+                                                         : __ldg(p.t_img + (int64_t)b * p.N + (kj - L));
+                                vis = tj == t_row;
+                            }
+                        }
+                        keep |= (uint64_t)vis << c;
+                    }
+                }
+            }
+            // Full mask: only keys past the segment's end are hidden (a plain
+            // compare, cheaper in the hot loops than testing a bit of `keep`).
+            auto visible = [&](int c) -> bool {
+                if constexpr (block_causal) return (keep >> c) & 1u;
+                else return c < valid;
+            };
             float* mx_tile = mx_s + (j & 1) * 256;
             if (ok) {
                 tc_fence_after();
@@ -307,7 +349,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 // Keys past the end of the prefix or image segment do not exist.
                 if (partial) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                    for (int c = 0; c < 64; ++c) s[c] = visible(c) ? s[c] : -INFINITY;
                 }
                 // Partial row maximum of the raw logits (three-input max tree).
                 float t1[22];
@@ -366,8 +408,8 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             for (int c = 0; c < 32; ++c) {
                 float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
                 if (partial) {
-                    a.x = 2 * c < valid ? a.x : -INFINITY;
-                    a.y = 2 * c + 1 < valid ? a.y : -INFINITY;
+                    a.x = visible(2 * c) ? a.x : -INFINITY;
+                    a.y = visible(2 * c + 1) ? a.y : -INFINITY;
                 }
                 const float2 e = make_float2(ex2(a.x), ex2(a.y));
                 acc[c & 3] = fadd2(acc[c & 3], e);
@@ -501,8 +543,6 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
                                         int B, int N, int Hq, int Hkv, int D, neo_mask mask_mode,
                                         const int32_t* t_prefix, const int32_t* t_img, float scale, void* out,
                                         float* lse, cudaStream_t stream) {
-    (void)t_prefix;
-    (void)t_img;
     if (D != 128 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return NEO_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
     if (kBlockM % G != 0) return NEO_ERR_UNSUPPORTED;
@@ -515,7 +555,7 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return NEO_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || scale < 0.f) return NEO_ERR_INVALID_ARG;
     if (mask_mode != NEO_MASK_FULL && mask_mode != NEO_MASK_BLOCK_CAUSAL) return NEO_ERR_INVALID_ARG;
-    if (mask_mode == NEO_MASK_BLOCK_CAUSAL) return NEO_ERR_UNSUPPORTED;
+    if (mask_mode == NEO_MASK_BLOCK_CAUSAL && (!t_img || (total_prefix > 0 && !t_prefix))) return NEO_ERR_INVALID_ARG;
     if (dtype != NEO_BF16) return NEO_ERR_UNSUPPORTED;
     if (B > 65535 || Hkv > 65535) return NEO_ERR_UNSUPPORTED;
 
@@ -550,13 +590,19 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gen_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gen_attention_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(gen_attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kSmemBytes);
     });
     if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
 
     AttnParams prm;
     prm.cu_prefix = cu_prefix;
+    prm.t_prefix = t_prefix;
+    prm.t_img = t_img;
+    prm.mask_mode = (int)mask_mode;
     prm.lse = lse;
     prm.total_prefix = total_prefix;
     prm.B = B;
@@ -572,6 +618,9 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     // computes and stores nothing of its own but still shares the K/V stream).
     const int qtiles = (N + tok_per_tile - 1) / tok_per_tile;
     const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
-    gen_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
+    if (mask_mode == NEO_MASK_BLOCK_CAUSAL)
+        gen_attention_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
+    else
+        gen_attention_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
     return neo::launch_status();
 }

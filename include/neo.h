@@ -126,9 +126,14 @@ neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype,
  *   the device: a violation sets NEO_DEVERR_BAD_PREFIX and the affected
  *   sequence's output is left unwritten). A length of 0 is allowed.
  * D must be 128; Hq must be a multiple of Hkv and 128 a multiple of Hq/Hkv.
- * mask_mode: NEO_MASK_FULL. NEO_MASK_BLOCK_CAUSAL ([U15] section
- *   "Block-causal attention") needs t_prefix [total_prefix] and t_img [B*N]
- *   (int32 temporal indexes) and currently returns NEO_ERR_UNSUPPORTED.
+ * mask_mode: NEO_MASK_FULL, or NEO_MASK_BLOCK_CAUSAL ([U15] section
+ *   "Block-causal attention"): in the concatenated order [prefix_b ; image_b]
+ *   key j is visible to query i (i = L_b + n) iff T_j == T_i or j <= i, with
+ *   T the temporal index (indexes[0]) from t_prefix (device int32
+ *   [total_prefix], may be NULL when total_prefix == 0) and t_img (device
+ *   int32 [B*N]); both are ignored in NEO_MASK_FULL. A mixed prefill passes
+ *   its tokens as the image segment with L_b = 0 (or a cached chunk as the
+ *   prefix). Missing temporal indexes return NEO_ERR_INVALID_ARG.
  * scale: logit scale (1/sqrt(128) in the model), finite and >= 0.
  * out: [B, N, Hq, D] bf16. lse: optional fp32 [B, Hq, N] natural-log
  *   sum of exp(logits) per query row, or NULL.

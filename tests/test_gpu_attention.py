@@ -83,12 +83,69 @@ def test_attention_bad_cu_prefix_sets_device_error(gpu_lib):
     assert st == neo.NEO_OK and word == 0
 
 
-def test_block_causal_mode_is_reported_unsupported(gpu_lib):
+def _block_causal_case(prefix_T, img_T, Hq=8, Hkv=2, seed=0, scale=SCALE):
+    """prefix_T / img_T: per sequence, the temporal index of every prefix row
+    and every query (image-segment) token."""
+    B = len(img_T)
+    N = len(img_T[0])
+    Ls = [len(t) for t in prefix_T]
+    g = torch.Generator().manual_seed(seed)
+    bf = lambda *sh: torch.randn(*sh, generator=g).to(torch.bfloat16)
+    total = sum(Ls)
+    q, k, v = bf(B, N, Hq, 128), bf(B, N, Hkv, 128), bf(B, N, Hkv, 128)
+    kp, vp = bf(total, Hkv, 128), bf(total, Hkv, 128)
+    cu = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    t_pre = np.concatenate([np.asarray(t, np.int32) for t in prefix_T]) if total else np.zeros(0, np.int32)
+    t_img = np.asarray(img_T, np.int32)
+    out = torch.full((B, N, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    neo.neo_gen_attention(q.cuda(), kp.cuda() if total else None, vp.cuda() if total else None, k.cuda(), v.cuda(),
+                          torch.from_numpy(cu).cuda(), max(Ls), out, scale=scale,
+                          mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
+                          t_prefix=torch.from_numpy(t_pre).cuda() if total else None,
+                          t_img=torch.from_numpy(t_img.reshape(-1)).cuda())
+    ref, _ = O.gen_attention(f64(q), f64(kp), f64(vp), f64(k), f64(v), cu, scale, mask_mode=1,
+                             t_prefix=t_pre, t_img=t_img)
+    assert_bf16_close(f64(out), ref, "block-causal")
+    return out
+
+
+def _mixed_T(text_a, grid, text_b, start=0):
+    """Temporal indices of text (distinct), one image block (shared), text."""
+    t = list(range(start, start + text_a))
+    t += [start + text_a] * grid
+    t += list(range(start + text_a + 1, start + text_a + 1 + text_b))
+    return t
+
+
+def test_block_causal_with_generation_positions_equals_full_mask(gpu_lib):
+    L, N = 150, 132
+    out_bc = _block_causal_case([list(range(L))] * 2, [[L] * N] * 2, seed=1)
+    # the same inputs under the full mask
+    full = run_case((L, L), N, 8, 2, seed=1)
+    assert torch.equal(out_bc, full)
+
+
+def test_block_causal_mixed_prefill(gpu_lib):
+    """A whole prefill as the query segment (L = 0): 40 text tokens, an 8x8
+    image block, 25 more text tokens; a second sequence with other lengths."""
+    t0 = _mixed_T(40, 64, 25)
+    t1 = _mixed_T(7, 64, 58)
+    assert len(t0) == len(t1) == 129
+    _block_causal_case([[], []], [t0, t1], seed=2)
+
+
+def test_block_causal_chunked_prefill(gpu_lib):
+    """The first 70 tokens are a cached prefix, the next 130 are the queries;
+    the image block straddles the chunk boundary in the second sequence."""
+    a = _mixed_T(30, 100, 70)      # 200 tokens
+    b = _mixed_T(60, 64, 76)       # 200 tokens
+    _block_causal_case([a[:70], b[:70]], [a[70:], b[70:]], seed=3, Hq=4, Hkv=1)
+
+
+def test_block_causal_needs_temporal_indices(gpu_lib):
     q = torch.zeros(1, 8, 4, 128, dtype=torch.bfloat16, device="cuda")
     k = torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16, device="cuda")
     cu = torch.zeros(2, dtype=torch.int32, device="cuda")
-    t = torch.zeros(8, dtype=torch.int32, device="cuda")
     with pytest.raises(neo.NeoError) as e:
-        neo.neo_gen_attention(q, None, None, k, k, cu, 0, q.clone(), mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
-                              t_img=t)
-    assert e.value.status == neo.NEO_ERR_UNSUPPORTED
+        neo.neo_gen_attention(q, None, None, k, k, cu, 0, q.clone(), mask_mode=neo.NEO_MASK_BLOCK_CAUSAL)
+    assert e.value.status == neo.NEO_ERR_INVALID_ARG

@@ -40,6 +40,7 @@
 //     of O / l as bf16 through shared memory and a TMA store.
 // TMEM: S0 [0,128) S1 [128,256) S2 [256,384) O [384,512).
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -93,7 +94,18 @@ enum : int {
 constexpr uint32_t kSmTmemSlot = kSmBar + NUM_BARS * 8;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
 constexpr uint32_t kSmEpiSkip = kSmAbort + 4;   // written only by the softmax warps
-constexpr uint32_t kSmUsed = kSmEpiSkip + 4;
+// Block-causal mode: the queries' temporal-index range, the image tiles past
+// the diagonal that are kept (bitmask, then compacted into a list), their
+// count, and the [min, max] temporal index of each 64-key half of every image
+// tile from the cluster's first query tile on.
+constexpr int kMaxImgTiles = 1024;                 // image segment of at most 131072 tokens
+constexpr uint32_t kSmTRange = kSmEpiSkip + 4;     // int [2]
+constexpr uint32_t kSmNExtra = kSmTRange + 8;
+constexpr uint32_t kSmTileBits = kSmNExtra + 4;    // uint32 [kMaxImgTiles / 32]
+constexpr uint32_t kSmTileList = kSmTileBits + kMaxImgTiles / 8;   // uint16 [kMaxImgTiles]
+constexpr uint32_t kSmTileT = kSmTileList + kMaxImgTiles * 2;      // int4 [kMaxImgTiles]: min0 max0 min1 max1
+constexpr uint32_t kSmUsed = kSmTileT + kMaxImgTiles * 16;
+static_assert(kSmTileT % 16 == 0, "int4 entries need 16-byte alignment");
 constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 
@@ -142,8 +154,26 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     const int n_pre = (L + kBlockN - 1) / kBlockN;
     const int n_img = (p.N + kBlockN - 1) / kBlockN;
-    const int n_tiles = n_pre + n_img;
+    int n_tiles = n_pre + n_img;
     const int n0 = qt * p.tok_per_tile;
+
+    // Block-causal mode ("Block-causal attention"): image key tile t is needed
+    // by the cluster's queries [np0, np1) if it holds a key at or before the
+    // last of them (j <= i), or a key whose temporal index lies within the
+    // queries' [min, max] range (a superset of T_j == T_i). Tiles past the
+    // diagonal that fail the second test are masked for every row and are
+    // skipped by all roles; inside every tile kept the per-element mask still
+    // decides. Both CTAs of a cluster derive the same list, so they keep
+    // sharing one K/V stream.
+    [[maybe_unused]] const int np0 = (qt & ~(kCluster - 1)) * p.tok_per_tile;
+    [[maybe_unused]] const int np1 = min(p.N, np0 + kCluster * p.tok_per_tile);
+    [[maybe_unused]] const int j_diag = (np1 - 1) / kBlockN;
+    [[maybe_unused]] const uint16_t* tile_list = reinterpret_cast<const uint16_t*>(smem + kSmTileList);
+    // Position u of the image part of the tile sequence -> image tile index.
+    auto img_tile = [&](int u) -> int {
+        if constexpr (kBlockCausal) return u <= j_diag ? u : (int)tile_list[u - j_diag - 1];
+        else return u;
+    };
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmAbort);
     volatile int* epi_skip = reinterpret_cast<volatile int*>(smem + kSmEpiSkip);
@@ -167,6 +197,25 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         tmem_alloc(sb + kSmTmemSlot, kTmCols);
         tmem_relinquish();
     }
+    if constexpr (kBlockCausal) {
+        if (warp == 3) {
+            int tmin = INT_MAX, tmax = INT_MIN;
+            for (int n = np0 + lane; n < np1; n += 32) {
+                const int t = __ldg(p.t_img + (int64_t)b * p.N + n);
+                tmin = min(tmin, t);
+                tmax = max(tmax, t);
+            }
+            tmin = __reduce_min_sync(0xffffffffu, tmin);
+            tmax = __reduce_max_sync(0xffffffffu, tmax);
+            if (lane == 0) {
+                reinterpret_cast<int*>(smem + kSmTRange)[0] = tmin;
+                reinterpret_cast<int*>(smem + kSmTRange)[1] = tmax;
+            }
+        } else if (warp >= 4) {
+            for (int i = (int)threadIdx.x - 128; i < kMaxImgTiles / 32; i += kThreads - 128)
+                reinterpret_cast<uint32_t*>(smem + kSmTileBits)[i] = 0u;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     // No CTA may multicast into a peer before the peer's barriers exist.
@@ -174,6 +223,61 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSmTmemSlot);
     const uint32_t crank = cluster_ctarank();
+
+    if constexpr (kBlockCausal) {
+        // One warp per image tile from the one holding the cluster's first
+        // query on: the temporal-index range of each 64-key half, and for tiles
+        // past the diagonal whether any key's index lies in the queries' range.
+        const int tmin = reinterpret_cast<const int*>(smem + kSmTRange)[0];
+        const int tmax = reinterpret_cast<const int*>(smem + kSmTRange)[1];
+        uint32_t* bits = reinterpret_cast<uint32_t*>(smem + kSmTileBits);
+        int4* tile_t = reinterpret_cast<int4*>(smem + kSmTileT);
+        for (int t = np0 / kBlockN + warp; t < n_img; t += kThreads / 32) {
+            bool hit = false;
+            int lo2[2] = {INT_MAX, INT_MAX}, hi2[2] = {INT_MIN, INT_MIN};
+#pragma unroll
+            for (int c = 0; c < kBlockN / 32; ++c) {
+                const int key = t * kBlockN + c * 32 + lane;
+                if (key < p.N) {
+                    const int tk = __ldg(p.t_img + (int64_t)b * p.N + key);
+                    hit |= tk >= tmin && tk <= tmax;
+                    lo2[c >> 1] = min(lo2[c >> 1], tk);
+                    hi2[c >> 1] = max(hi2[c >> 1], tk);
+                }
+            }
+            const int4 range = make_int4(__reduce_min_sync(0xffffffffu, lo2[0]), __reduce_max_sync(0xffffffffu, hi2[0]),
+                                         __reduce_min_sync(0xffffffffu, lo2[1]), __reduce_max_sync(0xffffffffu, hi2[1]));
+            if (lane == 0) tile_t[t] = range;
+            if (t > j_diag && __any_sync(0xffffffffu, hit) && lane == 0) atomicOr(bits + (t >> 5), 1u << (t & 31));
+        }
+        __syncthreads();
+        // Compact the kept tiles, in ascending order, into the list.
+        if (warp == 0) {
+            uint16_t* list = reinterpret_cast<uint16_t*>(smem + kSmTileList);
+            const int n_words = (n_img + 31) >> 5;
+            int base = 0;
+            for (int w0 = (j_diag + 1) >> 5; w0 < n_words; w0 += 32) {
+                const int w = w0 + lane;
+                uint32_t rem = w < n_words ? bits[w] : 0u;
+                const int cnt = __popc(rem);
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                int pos = base + incl - cnt;
+                while (rem) {
+                    list[pos++] = (uint16_t)(w * 32 + __ffs(rem) - 1);
+                    rem &= rem - 1;
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) *reinterpret_cast<int*>(smem + kSmNExtra) = base;
+        }
+        __syncthreads();
+        n_tiles = n_pre + j_diag + 1 + *reinterpret_cast<const int*>(smem + kSmNExtra);
+    }
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers: K (warp 0) and V (warp 2)
@@ -206,7 +310,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 if (j < n_pre) {
                     tma_load_3d_mc(hdst, pre_map, fb, d0, kvh, lo + j * kBlockN, kClusterMask);
                 } else {
-                    tma_load_4d_mc(hdst, img_map, fb, d0, kvh, (j - n_pre) * kBlockN, b, kClusterMask);
+                    tma_load_4d_mc(hdst, img_map, fb, d0, kvh, img_tile(j - n_pre) * kBlockN, b, kClusterMask);
                 }
                 issued = j + 1;
             }
@@ -297,7 +401,6 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int n_row = min(n0 + row / p.G, p.N - 1);
         const int i_row = L + n_row;
         const int t_row = block_causal ? __ldg(p.t_img + (int64_t)b * p.N + n_row) : 0;
-        const int i_first = L + n0;                         // smallest query index of the tile
         // A failed (timed-out or aborted) wait sets `failed`. The loop then keeps
         // running without touching TMEM or the pipeline barriers, so that the
         // two warps of a row pair still meet at every pair barrier.
@@ -307,29 +410,35 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bool ok = !failed && __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + sbuf), (uint32_t)(j / kSBufs) & 1u));
             float s[64];
             float pmax = -INFINITY;
-            const int tile_valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - (j - n_pre) * kBlockN);
+            const int it = j < n_pre ? 0 : img_tile(j - n_pre);   // image tile index
+            const int tile_valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
             const int valid = tile_valid - half * 64;        // may be <= 0: this half is all padding
             // Concatenated index of this thread's first key column.
-            const int key0 = (j < n_pre ? j * kBlockN : L + (j - n_pre) * kBlockN) + half * 64;
-            // A tile entirely at or below the tile's first query needs no block-causal mask.
-            const bool causal_here = block_causal && key0 + 63 > i_first;
-            const bool partial = valid < 64 || causal_here;
+            const int key0 = (j < n_pre ? j * kBlockN : L + it * kBlockN) + half * 64;
+            bool partial = valid < 64;
             uint64_t keep = 0;                               // bit c: key column c is visible
             if constexpr (block_causal) {
-                if (partial) {
-                    for (int c = 0; c < 64; ++c) {
-                        bool vis = c < valid;
-                        if (vis && causal_here) {
-                            const int kj = key0 + c;
-                            if (kj > i_row) {
-                                const int tj = j < n_pre ? __ldg(p.t_prefix + lo + kj)
-                                                         : __ldg(p.t_img + (int64_t)b * p.N + (kj - L));
-                                vis = tj == t_row;
-                            }
+                // Classify this row's 64 keys: all at or before the row (i) or all
+                // sharing its temporal index -> the segment-end mask only; the
+                // row's index outside the keys' range -> causal, a threshold;
+                // otherwise (a block boundary) key by key.
+                keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
+                if (j >= n_pre && key0 + 63 > i_row) {
+                    const int4 tr = reinterpret_cast<const int4*>(smem + kSmTileT)[it];
+                    const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
+                    if (!(klo == t_row && khi == t_row)) {
+                        const int lim = i_row - key0 + 1;       // columns c < lim are at or before the row
+                        const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
+                        if (t_row < klo || t_row > khi) {
+                            keep &= causal;
+                        } else {
+                            const int32_t* tk = p.t_img + (int64_t)b * p.N + (key0 - L);
+                            for (int c = max(lim, 0); c < min(valid, 64); ++c)
+                                if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
                         }
-                        keep |= (uint64_t)vis << c;
                     }
                 }
+                partial = keep != ~0ull;
             }
             // Full mask: only keys past the segment's end are hidden (a plain
             // compare, cheaper in the hot loops than testing a bit of `keep`).
@@ -556,6 +665,7 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     if (!std::isfinite(scale) || scale < 0.f) return NEO_ERR_INVALID_ARG;
     if (mask_mode != NEO_MASK_FULL && mask_mode != NEO_MASK_BLOCK_CAUSAL) return NEO_ERR_INVALID_ARG;
     if (mask_mode == NEO_MASK_BLOCK_CAUSAL && (!t_img || (total_prefix > 0 && !t_prefix))) return NEO_ERR_INVALID_ARG;
+    if (mask_mode == NEO_MASK_BLOCK_CAUSAL && (N + kBlockN - 1) / kBlockN > kMaxImgTiles) return NEO_ERR_UNSUPPORTED;
     if (dtype != NEO_BF16) return NEO_ERR_UNSUPPORTED;
     if (B > 65535 || Hkv > 65535) return NEO_ERR_UNSUPPORTED;
 

@@ -133,7 +133,10 @@ neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype,
  *   [total_prefix], may be NULL when total_prefix == 0) and t_img (device
  *   int32 [B*N]); both are ignored in NEO_MASK_FULL. A mixed prefill passes
  *   its tokens as the image segment with L_b = 0 (or a cached chunk as the
- *   prefix). Missing temporal indexes return NEO_ERR_INVALID_ARG.
+ *   prefix). Missing temporal indexes return NEO_ERR_INVALID_ARG; an image
+ *   segment of more than 131072 tokens returns NEO_ERR_UNSUPPORTED. Key
+ *   tiles that the mask hides from every query of a tile are skipped; any
+ *   temporal indexes are allowed (no ordering is assumed).
  * scale: logit scale (1/sqrt(128) in the model), finite and >= 0.
  * out: [B, N, Hq, D] bf16. lse: optional fp32 [B, Hq, N] natural-log
  *   sum of exp(logits) per query row, or NULL.

@@ -78,6 +78,7 @@ def _attn(lib, **kw):
     (dict(mask=7), neo.NEO_ERR_INVALID_ARG),
     (dict(mask=1), neo.NEO_ERR_INVALID_ARG),                       # block-causal without temporal indices
     (dict(mask=1, ti=FAKE), neo.NEO_ERR_INVALID_ARG),              # ... prefix rows need theirs too
+    (dict(mask=1, ti=FAKE, tp=FAKE, N=1024 * 128 + 1), neo.NEO_ERR_UNSUPPORTED),   # image segment too long
     (dict(dt=neo.NEO_F32), neo.NEO_ERR_UNSUPPORTED),
     (dict(Hq=3, Hkv=1), neo.NEO_ERR_UNSUPPORTED),
 ])

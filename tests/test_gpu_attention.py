@@ -149,3 +149,62 @@ def test_block_causal_needs_temporal_indices(gpu_lib):
     with pytest.raises(neo.NeoError) as e:
         neo.neo_gen_attention(q, None, None, k, k, cu, 0, q.clone(), mask_mode=neo.NEO_MASK_BLOCK_CAUSAL)
     assert e.value.status == neo.NEO_ERR_INVALID_ARG
+
+
+def test_block_causal_unordered_temporal_indices(gpu_lib):
+    """No ordering of the temporal indexes is assumed: an image block far down
+    the sequence carries the temporal index of an early text token, so early
+    queries see keys several tiles past their own position (tiles that a
+    causal skip would drop)."""
+    T = list(range(300)) + [5] * 100 + list(range(300, 500))   # 600 tokens
+    _block_causal_case([[]], [T], seed=4)
+
+
+def test_block_causal_random_temporal_indices(gpu_lib):
+    rng = np.random.default_rng(11)
+    pre = [rng.integers(0, 40, size=50).tolist(), rng.integers(0, 400, size=90).tolist()]
+    img = [rng.integers(0, 40, size=333).tolist(), rng.integers(0, 400, size=333).tolist()]
+    _block_causal_case(pre, img, seed=9)
+
+
+def test_block_causal_long_prefill_many_tiles(gpu_lib):
+    """35 image key tiles, G = 1: the kept-tile list spans two 32-tile words.
+    Text 300, a 64x64 image block, 4 more text tokens."""
+    _block_causal_case([[]], [_mixed_T(300, 4096, 4)], Hq=2, Hkv=2, seed=10)
+
+
+@pytest.mark.parametrize("chunk", [0, 2048])
+def test_block_causal_full_size_prefill_sampled_rows(gpu_lib, chunk):
+    """An editing prefill at full size: 256 text tokens, a 64x64 reference
+    image at temporal index 256, 512 more text tokens (4864 tokens, 32 Q /
+    8 KV heads); temporal indexes from the positions kernel. chunk = 0: the
+    whole prefill is the query segment; chunk = 2048: the first 2048 tokens
+    are a cached prefix (the image block straddles the boundary). 384 sampled
+    query rows are checked one by one against the oracle, with their LSE."""
+    segs = [("text", 0, 256), ("image", 256, 64, 64), ("text", 257, 512)]
+    S, Hq, Hkv = 4864, 32, 8
+    idx = torch.empty(3, S, dtype=torch.int32, device="cuda")
+    neo.neo_build_positions(idx, segs)
+    T = idx[0].contiguous()
+    g = torch.Generator().manual_seed(77)
+    bf = lambda *sh: torch.randn(*sh, generator=g).to(torch.bfloat16)
+    q, k, v = bf(S, Hq, 128), bf(S, Hkv, 128), bf(S, Hkv, 128)
+    L, N = chunk, S - chunk
+    qd = q[L:].unsqueeze(0).cuda()
+    kd, vd = k[L:].unsqueeze(0).cuda(), v[L:].unsqueeze(0).cuda()
+    kp, vp = (k[:L].cuda(), v[:L].cuda()) if L else (None, None)
+    cu = torch.tensor([0, L], dtype=torch.int32, device="cuda")
+    out = torch.full((1, N, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((1, Hq, N), float("nan"), device="cuda")
+    neo.neo_gen_attention(qd, kp, vp, kd, vd, cu, L, out, scale=SCALE, lse=lse, mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
+                          t_prefix=T[:L].contiguous() if L else None, t_img=T[L:].contiguous())
+    rng = np.random.default_rng(chunk)
+    flat = rng.choice(N * Hq, size=384, replace=False)
+    rows = np.stack([np.zeros_like(flat), flat // Hq, flat % Hq], axis=1)
+    Th = T.cpu().numpy()
+    ref, ref_lse = O.gen_attention(f64(qd.cpu()), f64(k[:L]), f64(v[:L]), f64(kd.cpu()), f64(vd.cpu()),
+                                   np.array([0, L]), SCALE, mask_mode=1, t_prefix=Th[:L], t_img=Th[L:][None],
+                                   rows=rows)
+    got = f64(out.cpu())[0, rows[:, 1], rows[:, 2]]
+    assert_bf16_close(got, ref, f"block-causal prefill chunk={chunk}")
+    np.testing.assert_allclose(f64(lse.cpu())[0, rows[:, 2], rows[:, 1]], ref_lse, rtol=1e-4, atol=1e-3)

@@ -7,6 +7,7 @@
 //          NEO-unify Architecture"
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -64,18 +65,23 @@ __global__ void positions_kernel(int32_t* __restrict__ idx, int64_t S, const Seg
 // ---------------------------------------------------------------------------
 // QK-norm on halves + three-axis RoPE ([U15] "Three rotary axes").
 //
-// Work item = one token and up to kHeadsPerItem of its q heads or of its k
-// heads (items never mix the two). A row of 128 values is owned by a group of
-// lanes in which every lane holds BOTH members of its rotation pairs: two
+// One warp per token and tensor: it normalises and rotates the token's Hq
+// query rows (or its Hkv key rows), so the (cos, sin) of the token's angles
+// are computed once per lane and serve all of them. A row of 128 values is owned by a group
+// of lanes in which every lane holds BOTH members of its rotation pairs: two
 // 16-byte chunks at dims [a, a+E) and [a+d/2, a+d/2+E) of its slice (E = 8
 // bf16 or 4 fp32), so the rotation needs no data exchange. Lanes [0, 32/E) of
-// the group cover the temporal slice [0,64) (= the first normalised half),
-// the others the height [64,96) and width [96,128) slices (= the second
-// half); the half's sum of squares is a shuffle reduction inside that aligned
-// lane group. Each lane computes the (cos, sin) of its E pairs once per item.
-// The CTAs are persistent; each warp keeps its next kNormDepth - 1 items in
-// flight with cp.async copies into a private shared-memory ring while the
-// current item is normalised, rotated and stored.
+// the group cover the temporal slice [0,64) (= the first normalised half), the
+// others the height [64,96) and width [96,128) slices (= the second half); a
+// half's sum of squares is a shuffle reduction inside that aligned lane group.
+// With the norm weight w folded into the angle's (cos, sin), a pair (u, v) of
+// a row with inverse RMS r becomes
+//   u' = r * (u * w_u * cos - v * w_v * sin),  v' = r * (v * w_v * cos + u * w_u * sin),
+// four products per lane and token kept in registers. The token's rows stream
+// through a private ring of kNormDepth chunks of kNormChunkRows rows in shared
+// memory, filled with cp.async: a lane copies exactly the bytes it later
+// reads, so its own wait_group is the only synchronisation. The arithmetic
+// runs on the packed fp32x2 datapath.
 // ---------------------------------------------------------------------------
 __device__ unsigned int g_elem_error = 0;
 __device__ unsigned long long g_elem_wait_limit_ns = 1000000000ull;
@@ -87,10 +93,9 @@ struct RopeFreqs {
     float lo[64];   // pairs [0,32) temporal, [32,48) height, [48,64) width
 };
 
-constexpr int kNormThreads = 256;
-constexpr int kNormCtasPerSm = 3;
-constexpr int kHeadsPerItem = 4;
-constexpr int kNormDepth = 2;
+constexpr int kNormWarps = 4;        // tokens per CTA, one per warp
+constexpr int kNormChunkRows = 8;    // rows per ring slot
+constexpr int kNormDepth = 3;        // ring slots per warp (24 rows in flight)
 
 // sin/cos of pos * f with f = hi + lo: the exact product pos * hi is reduced
 // modulo 2*pi by the two-constant Cody-Waite scheme (2*pi = C1 + C2, each
@@ -123,6 +128,16 @@ struct Chunk<__nv_bfloat16> {
             x[2 * i + 1] = f.y;
         }
     }
+    // Elements (2i, 2i+1) as one pair: a bf16 is the top half of an fp32.
+    static __device__ __forceinline__ void unpack2(uint4 u, float2 (&x)[4]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    }
+    static __device__ __forceinline__ uint4 pack2(const float2 (&y)[4]) {
+        return make_uint4(sm103::pack_bf16x2(y[0].x, y[0].y), sm103::pack_bf16x2(y[1].x, y[1].y),
+                          sm103::pack_bf16x2(y[2].x, y[2].y), sm103::pack_bf16x2(y[3].x, y[3].y));
+    }
     static __device__ __forceinline__ uint4 pack(const float (&y)[8]) {
         uint32_t w[4];
 #pragma unroll
@@ -144,25 +159,42 @@ struct Chunk<float> {
     static __device__ __forceinline__ uint4 pack(const float (&y)[4]) {
         return make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]), __float_as_uint(y[2]), __float_as_uint(y[3]));
     }
+    static __device__ __forceinline__ void unpack2(uint4 u, float2 (&x)[2]) {
+        x[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        x[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
+    static __device__ __forceinline__ uint4 pack2(const float2 (&y)[2]) {
+        return make_uint4(__float_as_uint(y[0].x), __float_as_uint(y[0].y), __float_as_uint(y[1].x),
+                          __float_as_uint(y[1].y));
+    }
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm)
+__global__ void __launch_bounds__(kNormWarps * 32)
 qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int Hkv,
                     const int32_t* __restrict__ idx,
                     const float* __restrict__ wq_t, const float* __restrict__ wq_hw,
                     const float* __restrict__ wk_t, const float* __restrict__ wk_hw,
-                    const __grid_constant__ RopeFreqs freqs, float eps, int64_t n_items) {
+                    const __grid_constant__ RopeFreqs freqs, float eps) {
+    using sm103::ffma2;
+    using sm103::fmul2;
     constexpr int E = Chunk<T>::E;
+    constexpr int P = E / 2;                 // element pairs per chunk
     constexpr int LPR = 64 / E;              // lanes per row (8 bf16, 16 fp32)
     constexpr int HALF_LANES = 32 / E;       // lanes per normalised half
-    constexpr int ROWS_PER_WARP = 32 / LPR;
+    constexpr int RPW = 32 / LPR;            // rows per warp instruction
+    constexpr int ROW_BYTES = 128 * (int)sizeof(T);
+    constexpr int CHUNK_BYTES = kNormChunkRows * ROW_BYTES;
+    static_assert(kNormChunkRows % RPW == 0, "a ring slot holds whole row groups");
 
     __shared__ __align__(16) float w_s[2][128];   // norm weights of the full head dim: q, k
+    extern __shared__ __align__(16) uint8_t ring_mem[];
 
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int sub = threadIdx.x % LPR;
-    // This lane's slice, first dims of its u and w chunks, first pair (table order).
+    const int sub = lane % LPR;
+    const int rslot = lane / LPR;
+    // This lane's slice, first dims of its u and v chunks, first pair (table order).
     int dim_a, half_w, pair0, axis;
     if (sub < HALF_LANES) {
         dim_a = sub * E; half_w = 32; pair0 = sub * E; axis = 0;
@@ -174,13 +206,7 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
         dim_a = 96 + m * E; half_w = 16; pair0 = 48 + m * E; axis = 2;
     }
     const int dim_b = dim_a + half_w;
-    float fh[E], fl[E];
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-        fh[j] = freqs.hi[pair0 + j];
-        fl[j] = freqs.lo[pair0 + j];
-    }
-    for (int e = threadIdx.x; e < 256; e += kNormThreads) {
+    for (int e = threadIdx.x; e < 256; e += kNormWarps * 32) {
         const int which = e >> 7, d = e & 127;
         const float* wt = which ? wk_t : wq_t;
         const float* wh = which ? wk_hw : wq_hw;
@@ -188,102 +214,97 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
         w_s[which][d] = present ? (d < 64 ? wt[d] : wh[d - 64]) : 0.f;
     }
     __syncthreads();
-
-    // Per token: ceil(Hq/R) q items, then ceil(Hkv/R) k items (R = kHeadsPerItem).
-    // The host guarantees n_items < 2^31.
-    const int q_items = (Hq + kHeadsPerItem - 1) / kHeadsPerItem;
-    const int k_items = (Hkv + kHeadsPerItem - 1) / kHeadsPerItem;
-    const uint32_t per_tok = (uint32_t)(q_items + k_items);
-    const uint32_t n_it = (uint32_t)n_items;
-    const uint32_t first = ((blockIdx.x * kNormThreads + threadIdx.x) >> 5) * ROWS_PER_WARP;
-    const uint32_t stride = ((gridDim.x * kNormThreads) >> 5) * ROWS_PER_WARP;
-    const uint32_t sub_item = (uint32_t)(lane / LPR);
-
-    // Each warp keeps kNormDepth items in flight with cp.async copies into its
-    // own ring of shared-memory slots; a lane copies exactly the chunks it
-    // later reads, so its own wait_group is the only synchronisation needed.
-    constexpr uint32_t SLOT_BYTES = ROWS_PER_WARP * kHeadsPerItem * 128 * sizeof(T);
-    extern __shared__ __align__(16) uint8_t ring_mem[];
-    uint8_t* ring = ring_mem + (size_t)(threadIdx.x >> 5) * kNormDepth * SLOT_BYTES;
-    const uint32_t lane_off = (uint32_t)(lane / LPR) * kHeadsPerItem * 128 * sizeof(T);
-
-    struct Item {
-        T* base;
-        int nh;
-        int is_k;
-        int64_t tok;
-    };
-    auto locate = [&](uint32_t wb) {
-        Item it;
-        const uint32_t item = wb + sub_item;
-        const bool active = item < n_it;
-        it.tok = active ? (int64_t)(item / per_tok) : 0;
-        const int c = active ? (int)(item % per_tok) : 0;
-        it.is_k = c >= q_items;
-        const int h0 = (it.is_k ? c - q_items : c) * kHeadsPerItem;
-        it.nh = active ? min(kHeadsPerItem, (it.is_k ? Hkv : Hq) - h0) : 0;
-        it.base = it.is_k ? k + (it.tok * Hkv + h0) * 128 : q + (it.tok * Hq + h0) * 128;
-        return it;
-    };
-    auto issue = [&](uint32_t wb, int slot) {
-        const Item it = locate(wb);
-        const uint32_t dst = sm103::smem_addr(ring + (size_t)slot * SLOT_BYTES + lane_off);
+    const int64_t tok = (int64_t)blockIdx.x * kNormWarps + warp;
+    if (tok >= S) return;
+    // blockIdx.y picks the tensor: the q rows and the k rows of a token are
+    // handled by different CTAs, so that each CTA streams one contiguous region.
+    const int which = Hq > 0 ? (int)blockIdx.y : 1;
+    const int R = which ? Hkv : Hq;          // the token's rows of that tensor
+    const int n_chunks = (R + kNormChunkRows - 1) / kNormChunkRows;
+    uint8_t* ring = ring_mem + (size_t)warp * kNormDepth * CHUNK_BYTES;
+    T* const rows = which ? k + tok * Hkv * 128 : q + tok * Hq * 128;
+    auto row_ptr = [&](int r) -> T* { return rows + r * 128; };
+    auto issue = [&](int c) {
+        if (c < n_chunks) {
+            const uint32_t slot = sm103::smem_addr(ring + (c % kNormDepth) * CHUNK_BYTES);
 #pragma unroll
-        for (int r = 0; r < kHeadsPerItem; ++r) {
-            if (r < it.nh) {
-                const uint32_t d = dst + (uint32_t)r * 128u * sizeof(T);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + dim_a * (uint32_t)sizeof(T)),
-                             "l"(it.base + r * 128 + dim_a) : "memory");
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + dim_b * (uint32_t)sizeof(T)),
-                             "l"(it.base + r * 128 + dim_b) : "memory");
+            for (int g = 0; g < kNormChunkRows / RPW; ++g) {
+                const int rr = g * RPW + rslot;
+                const int r = c * kNormChunkRows + rr;
+                if (r < R) {
+                    const T* src = row_ptr(r);
+                    const uint32_t d = slot + (uint32_t)(rr * ROW_BYTES);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + dim_a * (uint32_t)sizeof(T)),
+                                 "l"(src + dim_a) : "memory");
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + dim_b * (uint32_t)sizeof(T)),
+                                 "l"(src + dim_b) : "memory");
+                }
             }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");   // possibly empty: keeps the group count uniform
     };
-    auto process = [&](uint32_t wb, int slot) {
-        const Item it = locate(wb);
-        const float pos = it.nh > 0 ? (float)__ldg(idx + axis * S + it.tok) : 0.f;
-        float cs[E], sn[E];
 #pragma unroll
-        for (int j = 0; j < E; ++j) rope_sincos(pos, fh[j], fl[j], &sn[j], &cs[j]);
-        const uint8_t* src = ring + (size_t)slot * SLOT_BYTES + lane_off;
+    for (int c = 0; c < kNormDepth; ++c) issue(c);
+
+    // The token's angles for this lane's pairs, and the weight-folded products
+    // (w_u cos, -w_v sin) for u' and (w_v cos, w_u sin) for v', element pairs packed.
+    const float pos = (float)__ldg(idx + axis * S + tok);
+    float cs[E], sn[E];
 #pragma unroll
-        for (int r = 0; r < kHeadsPerItem; ++r) {
-            const uint8_t* rowp = src + r * 128 * sizeof(T);
-            const uint4 ua = *reinterpret_cast<const uint4*>(rowp + dim_a * sizeof(T));
-            const uint4 ub = *reinterpret_cast<const uint4*>(rowp + dim_b * sizeof(T));
-            float xa[E], xb[E];
-            Chunk<T>::unpack(ua, xa);
-            Chunk<T>::unpack(ub, xb);
-            float ss = 0.f;
+    for (int j = 0; j < E; ++j) rope_sincos(pos, freqs.hi[pair0 + j], freqs.lo[pair0 + j], &sn[j], &cs[j]);
+    float2 uc[P], vs[P], vc[P], us[P];
+    auto fold = [&](int which) {
+        const float* w = w_s[which];
 #pragma unroll
-            for (int j = 0; j < E; ++j) ss = fmaf(xa[j], xa[j], fmaf(xb[j], xb[j], ss));
+        for (int i = 0; i < P; ++i) {
+            const float wu0 = w[dim_a + 2 * i], wu1 = w[dim_a + 2 * i + 1];
+            const float wv0 = w[dim_b + 2 * i], wv1 = w[dim_b + 2 * i + 1];
+            uc[i] = make_float2(wu0 * cs[2 * i], wu1 * cs[2 * i + 1]);
+            vs[i] = make_float2(-wv0 * sn[2 * i], -wv1 * sn[2 * i + 1]);
+            vc[i] = make_float2(wv0 * cs[2 * i], wv1 * cs[2 * i + 1]);
+            us[i] = make_float2(wu0 * sn[2 * i], wu1 * sn[2 * i + 1]);
+        }
+    };
+    fold(which);
+
+    for (int c = 0; c < n_chunks; ++c) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kNormDepth - 1) : "memory");
+        const uint8_t* slot = ring + (c % kNormDepth) * CHUNK_BYTES;
+#pragma unroll
+        for (int g = 0; g < kNormChunkRows / RPW; ++g) {
+            const int rr = g * RPW + rslot;
+            const int r = c * kNormChunkRows + rr;
+            const bool live = r < R;
+            uint4 ua = make_uint4(0u, 0u, 0u, 0u), ub = ua;
+            if (live) {
+                ua = *reinterpret_cast<const uint4*>(slot + rr * ROW_BYTES + dim_a * (int)sizeof(T));
+                ub = *reinterpret_cast<const uint4*>(slot + rr * ROW_BYTES + dim_b * (int)sizeof(T));
+            }
+            float2 xa[P], xb[P];
+            Chunk<T>::unpack2(ua, xa);
+            Chunk<T>::unpack2(ub, xb);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < P; ++i) acc = ffma2(xa[i], xa[i], ffma2(xb[i], xb[i], acc));
+            float ss = acc.x + acc.y;
 #pragma unroll
             for (int m = 1; m < HALF_LANES; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
             const float rs = rsqrtf(ss * (1.0f / 64.0f) + eps);
-            float ya[E], yb[E];
+            const float2 rs2 = make_float2(rs, rs);
+            float2 ya[P], yb[P];
 #pragma unroll
-            for (int j = 0; j < E; ++j) {
-                const float u = xa[j] * rs * w_s[it.is_k][dim_a + j];
-                const float w = xb[j] * rs * w_s[it.is_k][dim_b + j];
-                ya[j] = fmaf(u, cs[j], -w * sn[j]);
-                yb[j] = fmaf(w, cs[j], u * sn[j]);
+            for (int i = 0; i < P; ++i) {
+                const float2 u = fmul2(xa[i], rs2), v = fmul2(xb[i], rs2);
+                ya[i] = ffma2(u, uc[i], fmul2(v, vs[i]));
+                yb[i] = ffma2(v, vc[i], fmul2(u, us[i]));
             }
-            if (r < it.nh) {
-                *reinterpret_cast<uint4*>(it.base + r * 128 + dim_a) = Chunk<T>::pack(ya);
-                *reinterpret_cast<uint4*>(it.base + r * 128 + dim_b) = Chunk<T>::pack(yb);
+            if (live) {
+                T* dst = row_ptr(r);
+                *reinterpret_cast<uint4*>(dst + dim_a) = Chunk<T>::pack2(ya);
+                *reinterpret_cast<uint4*>(dst + dim_b) = Chunk<T>::pack2(yb);
             }
         }
-    };
-
-#pragma unroll
-    for (int d = 0; d < kNormDepth; ++d) issue(first + (uint32_t)d * stride, d);
-    int slot = 0;
-    for (uint32_t wb = first; wb < n_it; wb += stride) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kNormDepth - 1) : "memory");
-        process(wb, slot);
-        issue(wb + (uint32_t)kNormDepth * stride, slot);   // the slot was just read by this lane only
-        slot = slot + 1 == kNormDepth ? 0 : slot + 1;
+        issue(c + kNormDepth);   // into the slot this lane just read
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
@@ -582,16 +603,10 @@ extern "C" neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype, int64_
         put(32 + i, f);
         put(48 + i, f);
     }
-    const int64_t n_items =
-        S * ((Hq + kHeadsPerItem - 1) / kHeadsPerItem + (Hkv + kHeadsPerItem - 1) / kHeadsPerItem);
-    if (n_items >= (int64_t)1 << 31) return NEO_ERR_UNSUPPORTED;
-    const int lpr = dtype == NEO_BF16 ? 8 : 16;   // lanes per row
-    const int64_t items_per_cta = kNormThreads / lpr;
-    const int64_t blocks =
-        std::min<int64_t>((n_items + items_per_cta - 1) / items_per_cta, (int64_t)sm_count() * kNormCtasPerSm);
-    // Ring of kNormDepth slots per warp, each holding one item per row group of the warp.
-    const size_t ring = (size_t)(kNormThreads / 32) * kNormDepth * kHeadsPerItem * 128 * 32 / lpr *
-                        (dtype == NEO_BF16 ? 2 : 4);
+    const int64_t blocks = (S + kNormWarps - 1) / kNormWarps;
+    if (blocks > INT32_MAX) return NEO_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)blocks, (Hq > 0 ? 1u : 0u) + (Hkv > 0 ? 1u : 0u));
+    const size_t ring = (size_t)kNormWarps * kNormDepth * kNormChunkRows * 128 * (dtype == NEO_BF16 ? 2 : 4);
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -604,13 +619,13 @@ extern "C" neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype, int64_
     });
     if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
     if (dtype == NEO_BF16) {
-        qknorm_rope3_kernel<__nv_bfloat16><<<(unsigned)blocks, kNormThreads, ring, stream>>>(
+        qknorm_rope3_kernel<__nv_bfloat16><<<grid, kNormWarps * 32, ring, stream>>>(
             static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), S, Hq, Hkv, indexes, q_norm_w,
-            q_norm_hw_w, k_norm_w, k_norm_hw_w, fr, eps, n_items);
+            q_norm_hw_w, k_norm_w, k_norm_hw_w, fr, eps);
     } else {
-        qknorm_rope3_kernel<float><<<(unsigned)blocks, kNormThreads, ring, stream>>>(
+        qknorm_rope3_kernel<float><<<grid, kNormWarps * 32, ring, stream>>>(
             static_cast<float*>(q), static_cast<float*>(k), S, Hq, Hkv, indexes, q_norm_w, q_norm_hw_w,
-            k_norm_w, k_norm_hw_w, fr, eps, n_items);
+            k_norm_w, k_norm_hw_w, fr, eps);
     }
     return neo::launch_status();
 }

@@ -356,8 +356,8 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// Packed pair arithmetic on the fp32x2 datapath: (a.x*b.x + c.x, a.y*b.y + c.y)
-// and (a.x + b.x, a.y + b.y), each with one rounding per lane.
+// Packed pair arithmetic on the fp32x2 datapath: (a.x*b.x + c.x, a.y*b.y + c.y),
+// (a.x + b.x, a.y + b.y) and (a.x*b.x, a.y*b.y), each with one rounding per lane.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     uint64_t r;
     asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
@@ -374,6 +374,17 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     asm("{\n\t.reg .b64 ra, rb;\n\t"
         "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
         "add.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+        "mul.rn.f32x2 %0, ra, rb;\n\t}"
         : "=l"(r) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     float2 d;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));

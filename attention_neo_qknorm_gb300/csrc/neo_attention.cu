@@ -51,6 +51,7 @@
 
 #include "neo.h"
 #include "neo_internal.h"
+#include "neo_rope.cuh"
 #include "sm103_ptx.cuh"
 
 using namespace sm103;
@@ -88,7 +89,8 @@ enum : int {
     BAR_P_FULL = BAR_S_FULL + kSBufs,
     BAR_PV_DONE = BAR_P_FULL + kSBufs,
     BAR_DRAIN = BAR_PV_DONE + kSBufs,
-    NUM_BARS = BAR_DRAIN + 1
+    BAR_Q_READY = BAR_DRAIN + 1,   // folded query norm/RoPE done (one arrival per softmax thread)
+    NUM_BARS = BAR_Q_READY + 1
 };
 
 constexpr uint32_t kSmTmemSlot = kSmBar + NUM_BARS * 8;
@@ -103,8 +105,9 @@ constexpr uint32_t kSmTRange = kSmEpiSkip + 4;     // int [2]
 constexpr uint32_t kSmNExtra = kSmTRange + 8;
 constexpr uint32_t kSmTileBits = kSmNExtra + 4;    // uint32 [kMaxImgTiles / 32]
 constexpr uint32_t kSmTileList = kSmTileBits + kMaxImgTiles / 8;   // uint16 [kMaxImgTiles]
-constexpr uint32_t kSmTileT = kSmTileList + kMaxImgTiles * 2;      // int4 [kMaxImgTiles]: min0 max0 min1 max1
-constexpr uint32_t kSmUsed = kSmTileT + kMaxImgTiles * 16;
+constexpr uint32_t kSmTileT = (kSmTileList + kMaxImgTiles * 2 + 15u) & ~15u;   // int4 [kMaxImgTiles]: min0 max0 min1 max1
+constexpr uint32_t kSmQnW = kSmTileT + kMaxImgTiles * 16;   // float [128]: folded query norm weights
+constexpr uint32_t kSmUsed = kSmQnW + 128 * 4;
 static_assert(kSmTileT % 16 == 0, "int4 entries need 16-byte alignment");
 constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
@@ -126,17 +129,118 @@ struct AttnParams {
     int64_t total_prefix;
     int B, N, Hq, Hkv, G, tok_per_tile, max_prefix;
     float scale_log2;
+    // Folded query norm + RoPE (null qn_idx: the queries arrive normalised).
+    const int32_t* qn_idx;     // [3, B*N] positions of the image tokens
+    const float* qn_w_t;       // [64] weights of dims [0,64)
+    const float* qn_w_hw;      // [64] weights of dims [64,128)
+    float qn_eps;
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, int i) { return sbase + kSmBar + 8u * i; }
 
-template <bool kBlockCausal>
+// Query norm on halves + three-axis RoPE of one 64-dim half of one Q row in
+// shared memory ("Three rotary axes"), in place. The tile is 128-byte swizzled:
+// 16-byte chunk c of row r sits at r * 128 + ((c ^ (r & 7)) << 4) of its half.
+// Half 0 holds the temporal slice, rotation pairs (i, i+32) = chunks (c, c+4);
+// half 1 the height slice, pairs (i, i+16) = chunks (0,2), (1,3), and the
+// width slice, chunks (4,6), (5,7). The four chunk pairs are taken in the
+// order, and with the arithmetic (fp32x2 sums of squares combined as
+// (s0 + s1) + (s2 + s3), norm weights folded into cos/sin), of the standalone
+// norm/RoPE kernel's bf16 path, so the normalised query has the same bits.
+// The 32 (cos, sin) of one 64-dim half of a row, in the lane-partial order
+// below (chunk pair s, element pair j -> index 8 s + j). They depend only on
+// the token's positions, so they are computed while the Q tile is in flight.
+template <int half>
+__device__ __forceinline__ void qnorm_rope_angles(const float pos[3], const neo::RopeFreqs& fr, float (&cs)[32],
+                                                  float (&sn)[32]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int pair0 = half ? (s < 2 ? 32 + 8 * s : 48 + 8 * (s - 2)) : 8 * s;
+        const float p_s = pos[half ? (s < 2 ? 1 : 2) : 0];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            neo::rope_sincos(p_s, fr.hi[pair0 + j], fr.lo[pair0 + j], &sn[8 * s + j], &cs[8 * s + j]);
+    }
+}
+
+// Query norm on halves + three-axis RoPE of one 64-dim half of one Q row in
+// shared memory ("Three rotary axes"), in place. The tile is 128-byte swizzled:
+// 16-byte chunk c of row r sits at r * 128 + ((c ^ (r & 7)) << 4) of its half.
+// Half 0 holds the temporal slice, rotation pairs (i, i+32) = chunks (c, c+4);
+// half 1 the height slice, pairs (i, i+16) = chunks (0,2), (1,3), and the
+// width slice, chunks (4,6), (5,7). The four chunk pairs are taken in the
+// order, and with the arithmetic (fp32x2 sums of squares combined as
+// (s0 + s1) + (s2 + s3), norm weights folded into cos/sin), of the standalone
+// norm/RoPE kernel's bf16 path, so the normalised query has the same bits.
+// w: this half's 64 weights (shared memory).
+template <int half>
+__device__ __forceinline__ void qnorm_rope_q_half(uint8_t* half_tile, int row, const float (&cs)[32],
+                                                  const float (&sn)[32], const float* w, float eps) {
+    uint8_t* rowp = half_tile + row * 128;
+    uint4 raw[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + ((c ^ (row & 7)) << 4));
+    auto unpack = [](uint4 u, float2 (&x)[4]) {
+        const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = make_float2(__uint_as_float(v[i] << 16), __uint_as_float(v[i] & 0xffff0000u));
+    };
+    // chunk pairs (a, b) of this half, in lane-partial order
+    constexpr int pa[4] = {0, 1, half ? 4 : 2, half ? 5 : 3};
+    constexpr int pb[4] = {half ? 2 : 4, half ? 3 : 5, 6, 7};
+    float part[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        float2 xa[4], xb[4];
+        unpack(raw[pa[s]], xa);
+        unpack(raw[pb[s]], xb);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = ffma2(xa[i], xa[i], ffma2(xb[i], xb[i], acc));
+        part[s] = acc.x + acc.y;
+    }
+    const float ss = (part[0] + part[1]) + (part[2] + part[3]);
+    const float rs = rsqrtf(ss * (1.0f / 64.0f) + eps);
+    const float2 rs2 = make_float2(rs, rs);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const float4* wa4 = reinterpret_cast<const float4*>(w + 8 * pa[s]);
+        const float4* wb4 = reinterpret_cast<const float4*>(w + 8 * pb[s]);
+        const float4 wa_lo = wa4[0], wa_hi = wa4[1], wb_lo = wb4[0], wb_hi = wb4[1];
+        const float wa[8] = {wa_lo.x, wa_lo.y, wa_lo.z, wa_lo.w, wa_hi.x, wa_hi.y, wa_hi.z, wa_hi.w};
+        const float wb[8] = {wb_lo.x, wb_lo.y, wb_lo.z, wb_lo.w, wb_hi.x, wb_hi.y, wb_hi.z, wb_hi.w};
+        float2 xa[4], xb[4];
+        unpack(raw[pa[s]], xa);
+        unpack(raw[pb[s]], xb);
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = 8 * s + 2 * i;
+            const float2 uc = make_float2(wa[2 * i] * cs[e], wa[2 * i + 1] * cs[e + 1]);
+            const float2 vs = make_float2(-wb[2 * i] * sn[e], -wb[2 * i + 1] * sn[e + 1]);
+            const float2 vc = make_float2(wb[2 * i] * cs[e], wb[2 * i + 1] * cs[e + 1]);
+            const float2 us = make_float2(wa[2 * i] * sn[e], wa[2 * i + 1] * sn[e + 1]);
+            const float2 u = fmul2(xa[i], rs2), v = fmul2(xb[i], rs2);
+            const float2 ya = ffma2(u, uc, fmul2(v, vs));
+            const float2 yb = ffma2(v, vc, fmul2(u, us));
+            oa[i] = pack_bf16x2(ya.x, ya.y);
+            ob[i] = pack_bf16x2(yb.x, yb.y);
+        }
+        *reinterpret_cast<uint4*>(rowp + ((pa[s] ^ (row & 7)) << 4)) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        *reinterpret_cast<uint4*>(rowp + ((pb[s] ^ (row & 7)) << 4)) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    }
+}
+
+// kQNorm: the query norm + RoPE is folded into the prologue (a separate
+// instantiation, so that the plain kernel's code is unchanged by it).
+template <bool kBlockCausal, bool kQNorm>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                      const __grid_constant__ CUtensorMap tm_kimg,
                      const __grid_constant__ CUtensorMap tm_vimg,
                      const __grid_constant__ CUtensorMap tm_kpre,
-                     const __grid_constant__ CUtensorMap tm_vpre, const AttnParams p) {
+                     const __grid_constant__ CUtensorMap tm_vpre, const __grid_constant__ neo::RopeFreqs qn_freqs,
+                     const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_addr(smem);
@@ -189,6 +293,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if ((i >= BAR_K_EMPTY && i < BAR_K_EMPTY + kKStages) || (i >= BAR_V_EMPTY && i < BAR_V_EMPTY + kVStages))
                 count = kCluster;                // released by the MMA of every CTA of the cluster
             if (i == BAR_DRAIN) count = 2;      // one commit from each MMA issuer
+            if (i == BAR_Q_READY) count = kSoftmaxThreads;
             mbar_init(bar_addr(sb, i), count);
         }
         fence_barrier_init();
@@ -333,7 +438,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bool ok = true;
             if (warp == 1) {
                 const uint32_t sQ = sb + kSmQ;
-                ok = wait(bar_addr(sb, BAR_Q_FULL), 0);
+                ok = wait(bar_addr(sb, kQNorm ? BAR_Q_READY : BAR_Q_FULL), 0);
                 tc_fence_after();
                 for (int j = 0; ok && j < n_tiles; ++j) {
                     const int st = j % kKStages;
@@ -393,6 +498,37 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         float m_used = -INFINITY;
         float l_part = 0.f;
         bool failed = false;
+        if constexpr (kQNorm) {
+            // Folded query norm + RoPE: thread t normalises and rotates one
+            // 64-dim half (t / 128) of Q row t % 128. The positions, weights and
+            // angles do not depend on Q, so they are prepared while the tile is
+            // in flight; the S issuer starts when all 256 threads have arrived.
+            const int t = (int)threadIdx.x - 128;
+            const int qrow = t & 127, qhalf = t >> 7;
+            const int64_t S = (int64_t)p.B * p.N;
+            float* w_s = reinterpret_cast<float*>(smem + kSmQnW);
+            if (t < 128) w_s[t] = t < 64 ? __ldg(p.qn_w_t + t) : __ldg(p.qn_w_hw + (t - 64));
+            const int64_t tok = (int64_t)b * p.N + min(n0 + qrow / p.G, p.N - 1);
+            float pos[3];
+#pragma unroll
+            for (int a = 0; a < 3; ++a) pos[a] = (float)__ldg(p.qn_idx + a * S + tok);
+            float cs[32], sn[32];
+            if (qhalf == 0)   // warp-uniform
+                qnorm_rope_angles<0>(pos, qn_freqs, cs, sn);
+            else
+                qnorm_rope_angles<1>(pos, qn_freqs, cs, sn);
+            named_barrier_sync(1, kSoftmaxThreads);   // the weights are in shared memory
+            if (wait(bar_addr(sb, BAR_Q_FULL), 0)) {
+                if (qhalf == 0)
+                    qnorm_rope_q_half<0>(smem + kSmQ, qrow, cs, sn, w_s, p.qn_eps);
+                else
+                    qnorm_rope_q_half<1>(smem + kSmQ + kHalfTile, qrow, cs, sn, w_s + 64, p.qn_eps);
+                fence_proxy_async_smem();   // generic-proxy writes, read next by tcgen05.mma
+                mbar_arrive(bar_addr(sb, BAR_Q_READY));
+            } else {
+                failed = true;
+            }
+        }
         // Block-causal mode (section "Block-causal attention"): key j of the
         // concatenated order [prefix ; image] is visible to query i iff
         // T_j == T_i or j <= i. This row's query is image token n (clamped for
@@ -646,12 +782,13 @@ neo_status attention_set_timeout(uint64_t ns) {
 
 }  // namespace neo
 
-extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix, const void* v_prefix,
-                                        const void* k_img, const void* v_img, neo_dtype dtype,
-                                        const int32_t* cu_prefix, int64_t total_prefix, int32_t max_prefix,
-                                        int B, int N, int Hq, int Hkv, int D, neo_mask mask_mode,
-                                        const int32_t* t_prefix, const int32_t* t_img, float scale, void* out,
-                                        float* lse, cudaStream_t stream) {
+namespace {
+
+neo_status launch_attention(const void* q_img, const void* k_prefix, const void* v_prefix, const void* k_img,
+                            const void* v_img, neo_dtype dtype, const int32_t* cu_prefix, int64_t total_prefix,
+                            int32_t max_prefix, int B, int N, int Hq, int Hkv, int D, neo_mask mask_mode,
+                            const int32_t* t_prefix, const int32_t* t_img, const neo_qnorm_params* qn,
+                            float scale, void* out, float* lse, cudaStream_t stream) {
     if (D != 128 || B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return NEO_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
     if (kBlockM % G != 0) return NEO_ERR_UNSUPPORTED;
@@ -668,6 +805,10 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     if (mask_mode == NEO_MASK_BLOCK_CAUSAL && (N + kBlockN - 1) / kBlockN > kMaxImgTiles) return NEO_ERR_UNSUPPORTED;
     if (dtype != NEO_BF16) return NEO_ERR_UNSUPPORTED;
     if (B > 65535 || Hkv > 65535) return NEO_ERR_UNSUPPORTED;
+    if (qn && (!qn->indexes || !qn->q_norm_w || !qn->q_norm_hw_w || !(qn->theta_t > 0.f) ||
+               !(qn->theta_hw > 0.f) || !std::isfinite(qn->theta_t) || !std::isfinite(qn->theta_hw) ||
+               !(qn->eps >= 0.f) || !std::isfinite(qn->eps)))
+        return NEO_ERR_INVALID_ARG;
 
     const int tok_per_tile = kBlockM / G;
     const uint64_t row = 128 * 2;   // bytes per head row
@@ -700,11 +841,13 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gen_attention_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(gen_attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kSmemBytes);
+        const void* kernels[4] = {(const void*)gen_attention_kernel<false, false>,
+                                  (const void*)gen_attention_kernel<true, false>,
+                                  (const void*)gen_attention_kernel<false, true>,
+                                  (const void*)gen_attention_kernel<true, true>};
+        for (const void* k : kernels)
+            if (attr_err == cudaSuccess)
+                attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     });
     if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
 
@@ -723,14 +866,43 @@ extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
     prm.tok_per_tile = tok_per_tile;
     prm.max_prefix = max_prefix;
     prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.qn_idx = qn ? qn->indexes : nullptr;
+    prm.qn_w_t = qn ? qn->q_norm_w : nullptr;
+    prm.qn_w_hw = qn ? qn->q_norm_hw_w : nullptr;
+    prm.qn_eps = qn ? qn->eps : 0.f;
+    const neo::RopeFreqs fr = qn ? neo::rope3_freqs(qn->theta_t, qn->theta_hw) : neo::RopeFreqs{};
 
     // Query tiles come in clusters of kCluster (a tile past the last token loads,
     // computes and stores nothing of its own but still shares the K/V stream).
     const int qtiles = (N + tok_per_tile - 1) / tok_per_tile;
     const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
-    if (mask_mode == NEO_MASK_BLOCK_CAUSAL)
-        gen_attention_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
-    else
-        gen_attention_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, prm);
+    const bool bc = mask_mode == NEO_MASK_BLOCK_CAUSAL;
+    auto kernel = bc ? (qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>)
+                     : (qn ? gen_attention_kernel<false, true> : gen_attention_kernel<false, false>);
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, fr, prm);
     return neo::launch_status();
+}
+
+}  // namespace
+
+extern "C" neo_status neo_gen_attention(const void* q_img, const void* k_prefix, const void* v_prefix,
+                                        const void* k_img, const void* v_img, neo_dtype dtype,
+                                        const int32_t* cu_prefix, int64_t total_prefix, int32_t max_prefix,
+                                        int B, int N, int Hq, int Hkv, int D, neo_mask mask_mode,
+                                        const int32_t* t_prefix, const int32_t* t_img, float scale, void* out,
+                                        float* lse, cudaStream_t stream) {
+    return launch_attention(q_img, k_prefix, v_prefix, k_img, v_img, dtype, cu_prefix, total_prefix, max_prefix, B,
+                            N, Hq, Hkv, D, mask_mode, t_prefix, t_img, nullptr, scale, out, lse, stream);
+}
+
+extern "C" neo_status neo_gen_attention_qnorm(const void* q_img_raw, const void* k_prefix, const void* v_prefix,
+                                              const void* k_img, const void* v_img, neo_dtype dtype,
+                                              const int32_t* cu_prefix, int64_t total_prefix, int32_t max_prefix,
+                                              int B, int N, int Hq, int Hkv, int D, neo_mask mask_mode,
+                                              const int32_t* t_prefix, const int32_t* t_img,
+                                              const neo_qnorm_params* qnorm, float scale, void* out, float* lse,
+                                              cudaStream_t stream) {
+    if (!qnorm) return NEO_ERR_INVALID_ARG;
+    return launch_attention(q_img_raw, k_prefix, v_prefix, k_img, v_img, dtype, cu_prefix, total_prefix, max_prefix,
+                            B, N, Hq, Hkv, D, mask_mode, t_prefix, t_img, qnorm, scale, out, lse, stream);
 }

@@ -17,9 +17,13 @@
 
 #include "neo.h"
 #include "neo_internal.h"
+#include "neo_rope.cuh"
 #include "sm103_ptx.cuh"
 
 namespace {
+
+using neo::RopeFreqs;
+using neo::rope_sincos;
 
 int sm_count() {
     static int n = 0;
@@ -86,32 +90,11 @@ __global__ void positions_kernel(int32_t* __restrict__ idx, int64_t S, const Seg
 __device__ unsigned int g_elem_error = 0;
 __device__ unsigned long long g_elem_wait_limit_ns = 1000000000ull;
 
-struct RopeFreqs {
-    // theta^(-2i/d) of each pair split as hi + lo: hi keeps 11 significant bits
-    // so that pos * hi is exact in fp32 for positions below 2^13.
-    float hi[64];
-    float lo[64];   // pairs [0,32) temporal, [32,48) height, [48,64) width
-};
 
 constexpr int kNormWarps = 4;        // tokens per CTA, one per warp
 constexpr int kNormChunkRows = 8;    // rows per ring slot
 constexpr int kNormDepth = 3;        // ring slots per warp (24 rows in flight)
 
-// sin/cos of pos * f with f = hi + lo: the exact product pos * hi is reduced
-// modulo 2*pi by the two-constant Cody-Waite scheme (2*pi = C1 + C2, each
-// fp32, products folded with fma), then the small product pos * lo is added
-// and the SFU evaluates sin/cos on the reduced argument in [-pi, pi].
-__device__ __forceinline__ void rope_sincos(float pos, float f_hi, float f_lo, float* sn, float* cs) {
-    constexpr float kTwoPiHi = 6.28318548202514648f;        // fp32(2*pi)
-    constexpr float kTwoPiLo = -1.7484556025237907e-07f;    // 2*pi - kTwoPiHi
-    constexpr float kInvTwoPi = 0.15915494309189535f;
-    const float a = pos * f_hi;
-    const float k = rintf(a * kInvTwoPi);
-    float r = fmaf(-k, kTwoPiHi, a);
-    r = fmaf(-k, kTwoPiLo, r);
-    r = fmaf(pos, f_lo, r);
-    __sincosf(r, sn, cs);
-}
 
 template <typename T>
 struct Chunk;    // one 16-byte chunk of a row
@@ -588,21 +571,7 @@ extern "C" neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype, int64_
     if (S == 0 || Hq + Hkv == 0) return NEO_OK;
     if (!indexes) return NEO_ERR_INVALID_ARG;
 
-    // theta^(-2i/d) per pair in double, split as hi (11 significant bits) + lo.
-    RopeFreqs fr;
-    auto put = [&fr](int at, double f) {
-        int e;
-        const double m = std::frexp(f, &e);                       // f = m * 2^e, m in [0.5, 1)
-        const double hi = std::ldexp(std::floor(m * 2048.0) / 2048.0, e);
-        fr.hi[at] = (float)hi;
-        fr.lo[at] = (float)(f - hi);
-    };
-    for (int i = 0; i < 32; ++i) put(i, std::pow((double)theta_t, -2.0 * i / 64.0));
-    for (int i = 0; i < 16; ++i) {
-        const double f = std::pow((double)theta_hw, -2.0 * i / 32.0);
-        put(32 + i, f);
-        put(48 + i, f);
-    }
+    const RopeFreqs fr = neo::rope3_freqs(theta_t, theta_hw);
     const int64_t blocks = (S + kNormWarps - 1) / kNormWarps;
     if (blocks > INT32_MAX) return NEO_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)blocks, (Hq > 0 ? 1u : 0u) + (Hkv > 0 ? 1u : 0u));

@@ -25,7 +25,8 @@ NEO_DEVERR_TIMEOUT, NEO_DEVERR_BAD_PREFIX = 0x1, 0x2
 NEO_CFG_NONE, NEO_CFG_TEXT, NEO_CFG_CLASSIC, NEO_CFG_DUAL = range(4)
 NEO_NOISE_RESOLUTION, NEO_NOISE_DYNAMIC, NEO_NOISE_DYNAMIC_SQRT, NEO_NOISE_CONSTANT = range(4)
 
-EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
+EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_gen_attention_qnorm",
+           "neo_flow_euler_step",
            "neo_flow_cfg_euler_step", "neo_time_schedule", "neo_noise_scale", "neo_scale_noise",
            "neo_rope2d_interleaved",
            "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version")
@@ -39,6 +40,11 @@ class NeoError(RuntimeError):
 
 class neo_pos_segment(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("a", ctypes.c_int32), ("b", ctypes.c_int32), ("c", ctypes.c_int32)]
+
+
+class neo_qnorm_params(ctypes.Structure):
+    _fields_ = [("indexes", ctypes.c_void_p), ("q_norm_w", ctypes.c_void_p), ("q_norm_hw_w", ctypes.c_void_p),
+                ("theta_t", ctypes.c_float), ("theta_hw", ctypes.c_float), ("eps", ctypes.c_float)]
 
 
 _lib = None
@@ -60,6 +66,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                      _f32, _f32, _f32, _vp]
     lib.neo_gen_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, c_int, _vp, _i64, _i32, c_int, c_int, c_int,
                                       c_int, c_int, c_int, _vp, _vp, _f32, _vp, _vp, _vp]
+    lib.neo_gen_attention_qnorm.argtypes = [_vp, _vp, _vp, _vp, _vp, c_int, _vp, _i64, _i32, c_int, c_int, c_int,
+                                            c_int, c_int, c_int, _vp, _vp, ctypes.POINTER(neo_qnorm_params), _f32,
+                                            _vp, _vp, _vp]
     lib.neo_flow_euler_step.argtypes = [_vp, _vp, _i64, _f32, _f32, _f32, _vp, _vp]
     lib.neo_flow_cfg_euler_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _f32, _f32, _f32, _f32, _f32, _f32, _f32,
                                             _vp, ctypes.POINTER(ctypes.c_int32), _vp]
@@ -172,6 +181,30 @@ def neo_gen_attention(q_img, k_prefix, v_prefix, k_img, v_img, cu_prefix, max_pr
         int(max_prefix), B, N, Hq, Hkv, D, int(mask_mode), _ptr(t_prefix, torch.int32, "t_prefix"),
         _ptr(t_img, torch.int32, "t_img"), float(scale), _ptr(out, what="out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream, q_img)), "neo_gen_attention")
+
+
+def neo_gen_attention_qnorm(q_img_raw, k_prefix, v_prefix, k_img, v_img, cu_prefix, max_prefix, out, indexes,
+                            q_norm_w, q_norm_hw_w, theta_t=5e6, theta_hw=1e4, eps=1e-6, scale=128 ** -0.5,
+                            mask_mode=NEO_MASK_FULL, t_prefix=None, t_img=None, lse=None, stream=None):
+    """neo_gen_attention with the query norm + RoPE folded in: q_img_raw
+    [B, N, Hq, 128] bf16 before the norm (left unchanged), indexes int32
+    [3, B*N] positions of the image tokens, q norm weights fp32 [64] each."""
+    B, N, Hq, D = q_img_raw.shape
+    Hkv = k_img.shape[2]
+    total_prefix = k_prefix.shape[0] if k_prefix is not None else 0
+    dt = _DT.get(q_img_raw.dtype)
+    if dt is None:
+        raise ValueError("q_img_raw must be bf16")
+    qn = neo_qnorm_params(_ptr(indexes, torch.int32, "indexes"), _ptr(q_norm_w, torch.float32, "q_norm_w"),
+                          _ptr(q_norm_hw_w, torch.float32, "q_norm_hw_w"), float(theta_t), float(theta_hw),
+                          float(eps))
+    _check(load_library().neo_gen_attention_qnorm(
+        _ptr(q_img_raw, what="q_img_raw"), _ptr(k_prefix if total_prefix else None, what="k_prefix"),
+        _ptr(v_prefix if total_prefix else None, what="v_prefix"), _ptr(k_img, what="k_img"),
+        _ptr(v_img, what="v_img"), dt, _ptr(cu_prefix, torch.int32, "cu_prefix"), int(total_prefix),
+        int(max_prefix), B, N, Hq, Hkv, D, int(mask_mode), _ptr(t_prefix, torch.int32, "t_prefix"),
+        _ptr(t_img, torch.int32, "t_img"), ctypes.byref(qn), float(scale), _ptr(out, what="out"),
+        _ptr(lse, torch.float32, "lse"), _stream(stream, q_img_raw)), "neo_gen_attention_qnorm")
 
 
 def neo_flow_euler_step(z, x0_hat, t, t_next, t_eps=0.02, v_out=None, stream=None):

@@ -56,16 +56,36 @@ class GenPassLayer:
     def norm_rope(self, stream=None):
         neo.neo_qknorm_rope3(self.q, self.k, self.idx_img, *self.wts[:4], stream=stream)
 
+    def norm_rope_k(self, stream=None):
+        """The keys only: the queries' norm + RoPE is folded into attention_qnorm."""
+        neo.neo_qknorm_rope3(None, self.k, self.idx_img, None, None, *self.wts[2:4], stream=stream)
+
     def attention(self, lse=True, stream=None):
         w = self.w
         neo.neo_gen_attention(self.q.view(w.B, w.N, w.Hq, w.D), self.k_prefix, self.v_prefix,
                               self.k.view(w.B, w.N, w.Hkv, w.D), self.v, self.cu, self.max_prefix, self.out,
                               scale=SCALE, lse=self.lse if lse else None, stream=stream)
 
+    def attention_qnorm(self, lse=True, stream=None):
+        """Attention over the raw queries (self.q, left unchanged), normalised
+        and rotated inside the attention kernel."""
+        w = self.w
+        neo.neo_gen_attention_qnorm(self.q.view(w.B, w.N, w.Hq, w.D), self.k_prefix, self.v_prefix,
+                                    self.k.view(w.B, w.N, w.Hkv, w.D), self.v, self.cu, self.max_prefix, self.out,
+                                    self.idx_img, self.wts[0], self.wts[1], scale=SCALE,
+                                    lse=self.lse if lse else None, stream=stream)
+
     def euler(self, t, t_next, t_eps=0.02, stream=None):
         neo.neo_flow_euler_step(self.z, self.x0, t, t_next, t_eps, stream=stream)
 
-    def step(self, t, t_next, stream=None):
-        self.norm_rope(stream)
-        self.attention(lse=False, stream=stream)
+    def step(self, t, t_next, stream=None, fused=False):
+        """Queries and keys normed in place, then attention and the Euler step;
+        fused: keys normed in place and the queries inside the attention
+        (self.q stays raw)."""
+        if fused:
+            self.norm_rope_k(stream)
+            self.attention_qnorm(lse=False, stream=stream)
+        else:
+            self.norm_rope(stream)
+            self.attention(lse=False, stream=stream)
         self.euler(t, t_next, stream=stream)

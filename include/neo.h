@@ -152,6 +152,46 @@ neo_status neo_gen_attention(const void* q_img, const void* k_prefix,
                              cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Generation attention with the query norm and RoPE folded in.
+ * The same result as neo_qknorm_rope3 on the queries (steps a1 + a2, [U15]
+ * section "Three rotary axes") followed by neo_gen_attention, in one launch:
+ * each query tile is normalised on its halves and rotated in shared memory
+ * right after it is loaded, so the normalised queries never go to memory.
+ * The arithmetic is that of neo_qknorm_rope3's bf16 path, so the attention
+ * sees the same query bits (the keys still go through neo_qknorm_rope3).
+ *
+ * q_img_raw: [B, N, Hq, D] bf16 queries before the norm (read only).
+ * qnorm (host pointer, read during the call):
+ *   indexes     device int32 [3, B*N]: positions of the image tokens, token
+ *               b*N + n (as neo_build_positions writes them);
+ *   q_norm_w, q_norm_hw_w  device fp32 [64] each: weights of dims [0,64)
+ *               and [64,128);
+ *   theta_t, theta_hw      rotary bases (5e6, 1e4), finite and > 0;
+ *   eps         finite and >= 0 (1e-6).
+ * Every other argument, the layouts and the errors are those of
+ * neo_gen_attention; a NULL qnorm or a NULL member returns
+ * NEO_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    const int32_t* indexes;
+    const float* q_norm_w;
+    const float* q_norm_hw_w;
+    float theta_t;
+    float theta_hw;
+    float eps;
+} neo_qnorm_params;
+
+neo_status neo_gen_attention_qnorm(const void* q_img_raw, const void* k_prefix,
+                                   const void* v_prefix, const void* k_img,
+                                   const void* v_img, neo_dtype dtype,
+                                   const int32_t* cu_prefix, int64_t total_prefix,
+                                   int32_t max_prefix, int B, int N, int Hq, int Hkv,
+                                   int D, neo_mask mask_mode,
+                                   const int32_t* t_prefix, const int32_t* t_img,
+                                   const neo_qnorm_params* qnorm, float scale,
+                                   void* out, float* lse, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * x0 -> velocity conversion and one Euler step, in place.
  * [U15] section "Flow matching without a VAE": the pixel head predicts x0
  * and the sampler forms v = (x0 - z) / max(1 - t, t_eps), then

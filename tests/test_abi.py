@@ -165,3 +165,19 @@ def test_rope2d_rejects_bad_arguments(lib):
     assert f(FAKE, neo.NEO_BF16, 1, 4, 4, 16, -1.0, None) == neo.NEO_ERR_INVALID_ARG
     assert f(MISALIGNED, neo.NEO_F32, 1, 4, 4, 16, 1e4, None) == neo.NEO_ERR_INVALID_ARG
     assert f(None, neo.NEO_F32, 0, 4, 4, 16, 1e4, None) == neo.NEO_OK
+
+
+def test_fused_attention_rejects_bad_qnorm(lib):
+    f = lib.neo_gen_attention_qnorm
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, neo.NEO_BF16, FAKE, 10, 10, 1, 64, 32, 8, 128, 0, None, None]
+    tail = [0.088, FAKE, None, None]
+    assert f(*args, None, *tail) == neo.NEO_ERR_INVALID_ARG                 # no qnorm parameters
+    good = dict(indexes=0x10000, q_norm_w=0x10000, q_norm_hw_w=0x10000, theta_t=5e6, theta_hw=1e4, eps=1e-6)
+    for bad in (dict(indexes=None), dict(q_norm_w=None), dict(q_norm_hw_w=None), dict(theta_t=0.0),
+                dict(theta_hw=float("inf")), dict(eps=-1e-6)):
+        qn = neo.neo_qnorm_params(**dict(good, **bad))
+        assert f(*args, ctypes.byref(qn), *tail) == neo.NEO_ERR_INVALID_ARG, bad
+    qn = neo.neo_qnorm_params(**good)
+    a = list(args)
+    a[13] = 64                                                             # D != 128 is still rejected
+    assert f(*a, ctypes.byref(qn), *tail) == neo.NEO_ERR_INVALID_ARG

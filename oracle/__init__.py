@@ -32,4 +32,5 @@ from .neo_oracle import (  # noqa: F401
     rope3,
     rope_slices,
     time_schedule,
+    write_prefix_cache,
 )

@@ -240,6 +240,32 @@ def gen_attention(q, k_prefix, v_prefix, k_img, v_img, cu_prefix, scale,
 # ---------------------------------------------------------------------------
 # a4: x0 -> velocity conversion and the Euler step
 # ---------------------------------------------------------------------------
+def write_prefix_cache(k_old, v_old, cu_old, k_new, v_new, n_new):
+    """Append a chunk of keys/values to a packed per-sequence prefix cache.
+
+    [U15] §Mixture of Transformers, item 1: the understanding pass (a prefill,
+    possibly in chunks) writes the keys/values of its tokens into a KV cache
+    that the generation passes then read. [U1] §4.4 (KV-cache reuse): the
+    prefix cache is laid out once in the [B, S, H, D] form the attention
+    reads; here that form is packed without padding, sequence b owning rows
+    cu[b] .. cu[b+1]-1.
+
+    k_old, v_old: [cu_old[B], Hkv, D]; k_new, v_new: [B, N, Hkv, D], of which
+    sequence b contributes its first n_new[b] rows (its chunk), in order,
+    after its old rows. Returns (k_out, v_out, cu_out).
+    """
+    cu_old = np.asarray(cu_old, np.int64)
+    B = len(cu_old) - 1
+    ks, vs, cu = [], [], [0]
+    for b in range(B):
+        lo, hi = int(cu_old[b]), int(cu_old[b + 1])
+        n = int(n_new[b])
+        ks += [np.asarray(k_old)[lo:hi], np.asarray(k_new)[b, :n]]
+        vs += [np.asarray(v_old)[lo:hi], np.asarray(v_new)[b, :n]]
+        cu.append(cu[-1] + (hi - lo) + n)
+    return np.concatenate(ks), np.concatenate(vs), np.asarray(cu, np.int64)
+
+
 def flow_euler_step(z, x0_hat, t, t_next, t_eps=0.02):
     """One sampler step of the pixel-space rectified flow.
 

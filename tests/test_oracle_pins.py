@@ -466,3 +466,64 @@ def test_rope2d_relative_position():
     dot = lambda a, b: float(np.sum(yq[0, a] * yk[0, b]))
     # (r, c) pairs with equal offsets give equal dot products
     assert dot(1 * cols + 2, 3 * cols + 5) == pytest.approx(dot(2 * cols + 1, 4 * cols + 4), rel=1e-10)
+
+
+# ------------------------------------------------------------------ prefix cache
+def _cache_case(rng, lens, N, n_new, Hkv=2, D=8):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    k_old = rng.standard_normal((int(cu[-1]), Hkv, D))
+    v_old = rng.standard_normal((int(cu[-1]), Hkv, D))
+    k_new = rng.standard_normal((len(lens), N, Hkv, D))
+    v_new = rng.standard_normal((len(lens), N, Hkv, D))
+    return k_old, v_old, cu, k_new, v_new, np.asarray(n_new)
+
+
+def test_cache_empty_chunk_leaves_the_cache():
+    rng = np.random.default_rng(0)
+    k_old, v_old, cu, k_new, v_new, n = _cache_case(rng, (3, 0, 5), 4, (0, 0, 0))
+    k, v, cu_out = O.write_prefix_cache(k_old, v_old, cu, k_new, v_new, n)
+    assert np.array_equal(k, k_old) and np.array_equal(v, v_old) and np.array_equal(cu_out, cu)
+
+
+def test_cache_from_empty_is_a_masked_gather():
+    """Appending to empty caches packs the valid rows of the chunk: the same
+    rows, in the same order, as boolean-mask indexing of the padded chunk."""
+    rng = np.random.default_rng(1)
+    k_old, v_old, cu, k_new, v_new, n = _cache_case(rng, (0, 0, 0), 6, (6, 2, 4))
+    k, v, cu_out = O.write_prefix_cache(k_old, v_old, cu, k_new, v_new, n)
+    mask = np.arange(6)[None, :] < n[:, None]
+    assert np.array_equal(k, k_new[mask]) and np.array_equal(v, v_new[mask])
+    assert list(cu_out) == [0, 6, 8, 12]
+
+
+def test_cache_two_appends_equal_one_append_of_the_joined_chunk():
+    rng = np.random.default_rng(2)
+    k_old, v_old, cu, k1, v1, n1 = _cache_case(rng, (2, 7), 3, (3, 1))
+    _, _, _, k2, v2, n2 = _cache_case(rng, (2, 7), 5, (2, 5))
+    ka, va, cua = O.write_prefix_cache(*O.write_prefix_cache(k_old, v_old, cu, k1, v1, n1), k2, v2, n2)
+    kj = np.zeros((2, 8) + k1.shape[2:])
+    vj = np.zeros_like(kj)
+    for b in range(2):
+        kj[b, :n1[b] + n2[b]] = np.concatenate([k1[b, :n1[b]], k2[b, :n2[b]]])
+        vj[b, :n1[b] + n2[b]] = np.concatenate([v1[b, :n1[b]], v2[b, :n2[b]]])
+    kb, vb, cub = O.write_prefix_cache(k_old, v_old, cu, kj, vj, n1 + n2)
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb) and np.array_equal(cua, cub)
+
+
+def test_chunked_block_causal_prefill_through_the_cache_equals_one_pass():
+    """Block-causal prefill of a sequence in one pass equals: prefill the
+    first chunk, write its keys/values to the cache, then prefill the second
+    chunk against that cache (the image block straddles the boundary)."""
+    rng = np.random.default_rng(3)
+    T = np.array(list(range(5)) + [5] * 9 + list(range(6, 10)))   # 18 tokens
+    S, Hq, Hkv, D = len(T), 4, 2, 16
+    q = rng.standard_normal((1, S, Hq, D))
+    k = rng.standard_normal((1, S, Hkv, D))
+    v = rng.standard_normal((1, S, Hkv, D))
+    empty = np.zeros((0, Hkv, D))
+    full, _ = O.gen_attention(q, empty, empty, k, v, [0, 0], 0.3, mask_mode=1, t_prefix=T[:0], t_img=T[None])
+    c = 8
+    kc, vc, cu = O.write_prefix_cache(empty, empty, [0, 0], k[:, :c], v[:, :c], [c])
+    second, _ = O.gen_attention(q[:, c:], kc, vc, k[:, c:], v[:, c:], cu, 0.3, mask_mode=1,
+                                t_prefix=T[:c], t_img=T[None, c:])
+    np.testing.assert_allclose(second, full[:, c:], rtol=1e-12, atol=1e-12)

@@ -503,6 +503,77 @@ rope2d_interleaved_kernel(T* __restrict__ x, int64_t n_tokens, int rows, int col
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefix-cache write ([U15] "Mixture of Transformers" item 1: the
+// understanding pass writes a KV cache; [U1] section 4.4: the prefix cache in
+// the [B, S, H, D] form the attention reads, here packed without padding).
+// Sequence b's rows of the output are its old rows followed by the first n_b
+// rows of its chunk. CTA (x, b) copies every gridDim.x-th row of sequence b
+// in 16-byte units; b's output offset is cu_old[b] plus the chunk rows of the
+// sequences before it, summed by the CTA (which also checks them).
+// ---------------------------------------------------------------------------
+constexpr int kCacheThreads = 128;
+
+__global__ void __launch_bounds__(kCacheThreads)
+write_prefix_cache_kernel(const uint4* __restrict__ k_old, const uint4* __restrict__ v_old,
+                          const int32_t* __restrict__ cu_old, int64_t total_old, const uint4* __restrict__ k_new,
+                          const uint4* __restrict__ v_new, const int32_t* __restrict__ n_new, int N, int row_u4,
+                          uint4* __restrict__ k_out, uint4* __restrict__ v_out, int32_t* __restrict__ cu_out,
+                          int64_t capacity, bool in_place) {
+    __shared__ long long red_sum[kCacheThreads / 32];
+    __shared__ int red_bad[kCacheThreads / 32];
+    const int b = blockIdx.y;
+    const int lo = cu_old[b], hi = cu_old[b + 1];
+    const int n = n_new ? n_new[b] : N;
+    long long before = 0;
+    int bad = 0;
+    for (int i = threadIdx.x; i < b; i += kCacheThreads) {
+        const int ni = n_new ? n_new[i] : N;
+        bad |= ni < 0 || ni > N;
+        before += ni;
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, m);
+        bad |= __shfl_xor_sync(0xffffffffu, bad, m);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red_sum[threadIdx.x >> 5] = before;
+        red_bad[threadIdx.x >> 5] = bad;
+    }
+    __syncthreads();
+    before = 0;
+    bad = 0;
+#pragma unroll
+    for (int w = 0; w < kCacheThreads / 32; ++w) {
+        before += red_sum[w];
+        bad |= red_bad[w];
+    }
+    const int64_t base = (int64_t)lo + before;
+    const int64_t old_rows = (int64_t)hi - lo;
+    const int64_t rows = old_rows + n;
+    if (bad || cu_old[0] != 0 || lo < 0 || hi < lo || hi > total_old || n < 0 || n > N || base + rows > capacity) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_elem_error, NEO_DEVERR_BAD_PREFIX);
+        return;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        cu_out[b + 1] = (int32_t)(base + rows);
+        if (b == 0) cu_out[0] = 0;
+    }
+    for (int64_t r = in_place ? old_rows + blockIdx.x : blockIdx.x; r < rows; r += gridDim.x) {
+        const bool old = r < old_rows;
+        const int64_t src = old ? (int64_t)lo + r : ((int64_t)b * N + (r - old_rows));
+        const uint4* ks = (old ? k_old : k_new) + src * row_u4;
+        const uint4* vs = (old ? v_old : v_new) + src * row_u4;
+        uint4* kd = k_out + (base + r) * row_u4;
+        uint4* vd = v_out + (base + r) * row_u4;
+        for (int c = threadIdx.x; c < row_u4; c += kCacheThreads) {
+            kd[c] = ks[c];
+            vd[c] = vs[c];
+        }
+    }
+}
+
 }  // namespace
 
 namespace neo {
@@ -697,5 +768,47 @@ extern "C" neo_status neo_rope2d_interleaved(void* x, neo_dtype dtype, int64_t n
     else
         rope2d_interleaved_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(static_cast<float*>(x), n_tokens,
                                                                                     rows, cols, C, log2_theta);
+    return neo::launch_status();
+}
+
+extern "C" neo_status neo_write_prefix_cache(const void* k_old, const void* v_old, const int32_t* cu_old,
+                                             int64_t total_old, const void* k_new, const void* v_new,
+                                             const int32_t* n_new, int B, int N, int Hkv, int D, neo_dtype dtype,
+                                             void* k_out, void* v_out, int32_t* cu_out, int64_t capacity,
+                                             cudaStream_t stream) {
+    if (D != 128 || B < 1 || N < 0 || Hkv < 1 || total_old < 0 || capacity < 0) return NEO_ERR_INVALID_ARG;
+    if (dtype != NEO_BF16 && dtype != NEO_F32) return NEO_ERR_INVALID_ARG;
+    if (!cu_old || !cu_out || !k_out || !v_out) return NEO_ERR_INVALID_ARG;
+    if (total_old > 0 && (!k_old || !v_old)) return NEO_ERR_INVALID_ARG;
+    if (N > 0 && (!k_new || !v_new)) return NEO_ERR_INVALID_ARG;
+    if (B > 65535 || capacity > 0x7fffffffLL || total_old > capacity) return NEO_ERR_UNSUPPORTED;
+    const void* ptrs[6] = {k_old, v_old, k_new, v_new, k_out, v_out};
+    for (const void* q : ptrs)
+        if (q && !neo::aligned16(q)) return NEO_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)Hkv * D * (dtype == NEO_BF16 ? 2 : 4);   // bytes per cache row
+    // The outputs may not overlap any input, except the in-place append of a
+    // single sequence (k_out == k_old and v_out == v_old).
+    const bool in_place = B == 1 && k_out == k_old && v_out == v_old && total_old > 0;
+    auto overlap = [](const void* a, int64_t an, const void* b, int64_t bn) {
+        if (!a || !b || an <= 0 || bn <= 0) return false;
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+        return a0 < b0 + (uintptr_t)bn && b0 < a0 + (uintptr_t)an;
+    };
+    const int64_t out_bytes = capacity * row, old_bytes = total_old * row, new_bytes = (int64_t)B * N * row;
+    const void* outs[2] = {k_out, v_out};
+    for (const void* o : outs) {
+        if (!in_place && (overlap(o, out_bytes, k_old, old_bytes) || overlap(o, out_bytes, v_old, old_bytes)))
+            return NEO_ERR_INVALID_ARG;
+        if (overlap(o, out_bytes, k_new, new_bytes) || overlap(o, out_bytes, v_new, new_bytes)) return NEO_ERR_INVALID_ARG;
+    }
+    if (overlap(k_out, out_bytes, v_out, out_bytes)) return NEO_ERR_INVALID_ARG;
+    if (in_place && (overlap(k_out, out_bytes, v_old, old_bytes) || overlap(v_out, out_bytes, k_old, old_bytes)))
+        return NEO_ERR_INVALID_ARG;
+    const int64_t want = ((int64_t)sm_count() * 8 + B - 1) / B;
+    const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, 4096));
+    write_prefix_cache_kernel<<<dim3(gx, (unsigned)B), kCacheThreads, 0, stream>>>(
+        static_cast<const uint4*>(k_old), static_cast<const uint4*>(v_old), cu_old, total_old,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), n_new, N, (int)(row / 16),
+        static_cast<uint4*>(k_out), static_cast<uint4*>(v_out), cu_out, capacity, in_place);
     return neo::launch_status();
 }

@@ -26,7 +26,7 @@ NEO_CFG_NONE, NEO_CFG_TEXT, NEO_CFG_CLASSIC, NEO_CFG_DUAL = range(4)
 NEO_NOISE_RESOLUTION, NEO_NOISE_DYNAMIC, NEO_NOISE_DYNAMIC_SQRT, NEO_NOISE_CONSTANT = range(4)
 
 EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_gen_attention_qnorm",
-           "neo_flow_euler_step",
+           "neo_write_prefix_cache", "neo_flow_euler_step",
            "neo_flow_cfg_euler_step", "neo_time_schedule", "neo_noise_scale", "neo_scale_noise",
            "neo_rope2d_interleaved",
            "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version")
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                             c_int, c_int, c_int, _vp, _vp, ctypes.POINTER(neo_qnorm_params), _f32,
                                             _vp, _vp, _vp]
     lib.neo_flow_euler_step.argtypes = [_vp, _vp, _i64, _f32, _f32, _f32, _vp, _vp]
+    lib.neo_write_prefix_cache.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp, _vp, c_int, c_int, c_int, c_int, c_int,
+                                           _vp, _vp, _vp, _i64, _vp]
     lib.neo_flow_cfg_euler_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _f32, _f32, _f32, _f32, _f32, _f32, _f32,
                                             _vp, ctypes.POINTER(ctypes.c_int32), _vp]
     lib.neo_time_schedule.argtypes = [_vp, c_int, _f32]
@@ -205,6 +207,24 @@ def neo_gen_attention_qnorm(q_img_raw, k_prefix, v_prefix, k_img, v_img, cu_pref
         int(max_prefix), B, N, Hq, Hkv, D, int(mask_mode), _ptr(t_prefix, torch.int32, "t_prefix"),
         _ptr(t_img, torch.int32, "t_img"), ctypes.byref(qn), float(scale), _ptr(out, what="out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream, q_img_raw)), "neo_gen_attention_qnorm")
+
+
+def neo_write_prefix_cache(k_old, v_old, cu_old, k_new, v_new, k_out, v_out, cu_out, n_new=None, stream=None):
+    """Append each sequence's first n_new[b] rows of k_new/v_new [B, N, Hkv, 128]
+    after its rows of the packed cache k_old/v_old [total_old, Hkv, 128]
+    (cu_old int32 [B+1]) into k_out/v_out [capacity, Hkv, 128]; cu_out int32
+    [B+1] receives the new offsets."""
+    B, N, Hkv, D = k_new.shape
+    total_old = k_old.shape[0] if k_old is not None else 0
+    dt = _DT.get(k_new.dtype)
+    if dt is None:
+        raise ValueError("k_new must be bf16 or fp32")
+    _check(load_library().neo_write_prefix_cache(
+        _ptr(k_old if total_old else None, what="k_old"), _ptr(v_old if total_old else None, what="v_old"),
+        _ptr(cu_old, torch.int32, "cu_old"), int(total_old), _ptr(k_new if N else None, what="k_new"),
+        _ptr(v_new if N else None, what="v_new"), _ptr(n_new, torch.int32, "n_new"), B, N, Hkv, D, dt,
+        _ptr(k_out, what="k_out"), _ptr(v_out, what="v_out"), _ptr(cu_out, torch.int32, "cu_out"),
+        int(k_out.shape[0]), _stream(stream, k_new)), "neo_write_prefix_cache")
 
 
 def neo_flow_euler_step(z, x0_hat, t, t_next, t_eps=0.02, v_out=None, stream=None):

@@ -192,6 +192,41 @@ neo_status neo_gen_attention_qnorm(const void* q_img_raw, const void* k_prefix,
                                    void* out, float* lse, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Append a chunk of keys/values to the packed prefix cache.
+ * [U15] section "Mixture of Transformers", item 1: the understanding pass
+ * (a prefill, possibly in chunks) writes the keys/values of its tokens into
+ * the KV cache that every generation pass then reads; [U1] section 4.4: the
+ * prefix cache is laid out once in the [B, S, H, D] form the attention
+ * reads, here packed without padding (the layout neo_gen_attention takes).
+ * The keys are expected already normalised and rotated (neo_qknorm_rope3
+ * with the prefill positions).
+ *
+ * k_old, v_old: [total_old, Hkv, D], sequence b owning rows cu_old[b] ..
+ *   cu_old[b+1]-1 (cu_old: device int32 [B+1], cu_old[0] = 0). NULL allowed
+ *   when total_old == 0.
+ * k_new, v_new: [B, N, Hkv, D]; sequence b appends its first n_new[b] rows
+ *   (n_new: device int32 [B], each in [0, N]; NULL means N for all).
+ * k_out, v_out: [capacity, Hkv, D]: sequence b's old rows, then its new rows,
+ *   packed in sequence order; cu_out: device int32 [B+1], written. The
+ *   outputs may not overlap the inputs, except that a single sequence (B = 1)
+ *   may append in place (k_out == k_old, v_out == v_old; its old rows are then
+ *   left untouched). dtype: NEO_BF16 or NEO_F32; D must be 128; pointers
+ *   16-byte aligned.
+ * Host-side errors: NEO_ERR_INVALID_ARG (sizes, pointers, overlap),
+ * NEO_ERR_UNSUPPORTED (B > 65535, capacity >= 2^31, total_old > capacity).
+ * Device-side: cu_old not ascending or beyond total_old, an n_new outside
+ * [0, N], or a result beyond capacity sets NEO_DEVERR_BAD_PREFIX and the
+ * affected sequence is not written.
+ * ------------------------------------------------------------------------ */
+neo_status neo_write_prefix_cache(const void* k_old, const void* v_old,
+                                  const int32_t* cu_old, int64_t total_old,
+                                  const void* k_new, const void* v_new,
+                                  const int32_t* n_new, int B, int N, int Hkv, int D,
+                                  neo_dtype dtype, void* k_out, void* v_out,
+                                  int32_t* cu_out, int64_t capacity,
+                                  cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * x0 -> velocity conversion and one Euler step, in place.
  * [U15] section "Flow matching without a VAE": the pixel head predicts x0
  * and the sampler forms v = (x0 - z) / max(1 - t, t_eps), then

@@ -181,3 +181,23 @@ def test_fused_attention_rejects_bad_qnorm(lib):
     a = list(args)
     a[13] = 64                                                             # D != 128 is still rejected
     assert f(*a, ctypes.byref(qn), *tail) == neo.NEO_ERR_INVALID_ARG
+
+
+def test_prefix_cache_write_rejects_bad_arguments(lib):
+    f = lib.neo_write_prefix_cache
+    A, Bp, C, Dp = V(0x100000), V(0x200000), V(0x300000), V(0x400000)   # disjoint, aligned, never dereferenced
+    args = dict(k_old=A, v_old=Bp, cu_old=FAKE, total_old=10, k_new=C, v_new=Dp, n_new=None, B=2, N=4, Hkv=1, D=128,
+                dt=neo.NEO_BF16, k_out=V(0x500000), v_out=V(0x600000), cu_out=FAKE, cap=64, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(*a.values())
+    assert call(D=64) == neo.NEO_ERR_INVALID_ARG
+    assert call(cu_old=None) == neo.NEO_ERR_INVALID_ARG
+    assert call(k_old=None) == neo.NEO_ERR_INVALID_ARG             # old rows but no buffer
+    assert call(k_new=MISALIGNED) == neo.NEO_ERR_INVALID_ARG
+    assert call(k_out=V(0x100000 + 256)) == neo.NEO_ERR_INVALID_ARG  # output overlaps the old keys
+    assert call(v_out=V(0x300000)) == neo.NEO_ERR_INVALID_ARG        # output overlaps the chunk
+    assert call(dt=7) == neo.NEO_ERR_INVALID_ARG
+    assert call(total_old=100) == neo.NEO_ERR_UNSUPPORTED             # more old rows than capacity
+    assert call(k_out=A, v_out=Bp) == neo.NEO_ERR_INVALID_ARG          # in place only for one sequence

@@ -40,6 +40,7 @@
 //     of O / l as bf16 through shared memory and a TMA store.
 // TMEM: S0 [0,128) S1 [128,256) S2 [256,384) O [384,512).
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -582,6 +583,9 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 if constexpr (block_causal) return (keep >> c) & 1u;
                 else return c < valid;
             };
+            // Warp-uniform, so that the per-element mask below is a branch that
+            // full tiles skip (with the full mask it depends on the tile only).
+            const bool masked = block_causal ? __any_sync(0xffffffffu, partial) : partial;
             float* mx_tile = mx_s + (j & 1) * 256;
             if (ok) {
                 tc_fence_after();
@@ -592,7 +596,10 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
                 }
                 // Keys past the end of the prefix or image segment do not exist.
-                if (partial) {
+                if (masked) {
+                    // An opaque statement keeps this block behind its branch: the
+                    // compiler would otherwise turn it into selects run on every tile.
+                    asm volatile("");
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = visible(c) ? s[c] : -INFINITY;
                 }
@@ -643,7 +650,9 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 }
             }
             // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU,
-            // four independent pair accumulators for the row sum.
+            // four independent pair accumulators for the row sum. A hidden key's
+            // logit is -inf and stays -inf here (the scale is > 0 and m finite
+            // from the first tile on), so its p is 0.
             const float2 cc = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm = make_float2(-m_used, -m_used);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -651,11 +660,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
-                if (partial) {
-                    a.x = visible(2 * c) ? a.x : -INFINITY;
-                    a.y = visible(2 * c + 1) ? a.y : -INFINITY;
-                }
+                const float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
                 const float2 e = make_float2(ex2(a.x), ex2(a.y));
                 acc[c & 3] = fadd2(acc[c & 3], e);
                 pk[c] = pack_bf16x2(e.x, e.y);
@@ -865,7 +870,10 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     prm.G = G;
     prm.tok_per_tile = tok_per_tile;
     prm.max_prefix = max_prefix;
-    prm.scale_log2 = scale * 1.4426950408889634f;
+    // A zero scale becomes a tiny positive one: every logit times it is then
+    // far below an ulp of the exponent (the same uniform softmax), and a hidden
+    // key's -inf logit stays -inf instead of becoming NaN.
+    prm.scale_log2 = std::max(scale * 1.4426950408889634f, 1e-30f);
     prm.qn_idx = qn ? qn->indexes : nullptr;
     prm.qn_w_t = qn ? qn->q_norm_w : nullptr;
     prm.qn_w_hw = qn ? qn->q_norm_hw_w : nullptr;

@@ -89,3 +89,61 @@ class GenPassLayer:
             self.norm_rope(stream)
             self.attention(lse=False, stream=stream)
         self.euler(t, t_next, stream=stream)
+
+
+class StreamedSteps:
+    """Steps whose inputs arrive from pinned host memory and whose results go
+    back to it, with the copies of one step overlapping the compute of its
+    neighbours.
+
+    Two request slots (each a GenPassLayer with its own device buffers) take
+    turns; slot s % 2 runs step s. Three streams: host-to-device copies of a
+    step's inputs (q, k, v, x0_hat), the step itself on the compute stream,
+    and device-to-host copies of its results (the attention output and z).
+    Events order every reuse of a buffer: a slot's inputs are overwritten only
+    after its previous step has computed, its compute waits for its inputs and
+    for the read-back of its previous results, and a read-back waits for the
+    compute. Plumbing only: the step is the same sequence of libneo calls.
+    """
+
+    def __init__(self, slots, h_inputs, h_outputs, fused=False):
+        """slots: two GenPassLayer; h_inputs: dict of pinned host tensors
+        q, k, v, x0 (shaped like the slot's buffers); h_outputs: per slot, a
+        dict of pinned host tensors out, z."""
+        assert len(slots) == 2 and len(h_outputs) == 2
+        self.slots, self.h_in, self.h_out, self.fused = slots, h_inputs, h_outputs, fused
+        dev = slots[0].q.device
+        self.s_in = torch.cuda.Stream(dev)
+        self.s_out = torch.cuda.Stream(dev)
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.loaded = [torch.cuda.Event() for _ in range(2)]
+        self.read = [torch.cuda.Event() for _ in range(2)]
+        self.started = [False, False]
+
+    def step(self, s, t, t_next):
+        i = s % 2
+        L = self.slots[i]
+        comp = torch.cuda.current_stream(L.q.device)
+        with torch.cuda.stream(self.s_in):
+            if self.started[i]:
+                self.s_in.wait_event(self.computed[i])
+            for name in ("q", "k", "v", "x0"):
+                getattr(L, name).copy_(self.h_in[name], non_blocking=True)
+            self.loaded[i].record(self.s_in)
+        comp.wait_event(self.loaded[i])
+        if self.started[i]:
+            comp.wait_event(self.read[i])
+        L.step(t, t_next, fused=self.fused)
+        self.computed[i].record(comp)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.computed[i])
+            self.h_out[i]["out"].copy_(L.out, non_blocking=True)
+            self.h_out[i]["z"].copy_(L.z, non_blocking=True)
+            self.read[i].record(self.s_out)
+        self.started[i] = True
+
+    def finish(self):
+        """Make the compute stream wait for every copy still in flight."""
+        comp = torch.cuda.current_stream(self.slots[0].q.device)
+        comp.wait_stream(self.s_in)
+        comp.wait_stream(self.s_out)

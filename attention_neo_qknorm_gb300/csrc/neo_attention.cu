@@ -729,6 +729,482 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
 }
 
+// --------------------------------------------------------------------- persistent
+// Persistent form of the full-mask kernel. A CTA's own work is 40 key tiles
+// at 2048^2, and a trace of the one-tile-per-CTA kernel showed ~6.7k cycles
+// before the first S and ~4k cycles of epilogue around ~56k cycles of tiles
+// (whose steady state runs near the tensor pipe's peak). Here each cluster of
+// two CTAs works through a sequence of units (a pair of neighbouring query
+// tiles of one sequence and KV head: one tile per CTA) and every role streams
+// straight from one unit into the next, so a unit's epilogue and the next
+// unit's first tiles overlap:
+//   * Q is double-buffered. The next unit's Q is loaded kQLead tiles before
+//     the current unit's last K tile; a unit's Q buffer becomes the staging
+//     buffer of its output once its last S has completed, and is refilled
+//     only after that output's store has read it (Q_EMPTY).
+//   * The next unit's first PV overwrites O only after every softmax thread
+//     has read the finished O (O_FREE).
+//   * K and V rings, S buffers and the pair exchange run on one tile counter
+//     across units. K has two stages here to make room for the second Q.
+// The softmax of a tile is the same as in gen_attention_kernel.
+namespace pk {
+
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kQLead = 4;                          // tiles ahead that the next Q is loaded
+
+constexpr uint32_t kSmQ0 = 0;                      // Q buffers 0 and 1 (also output staging)
+constexpr uint32_t kSmK = 2 * kTile;
+constexpr uint32_t kSmV = kSmK + kKStages * kTile;
+constexpr uint32_t kSmMax = kSmV + kVStages * kTile;   // float [2 tile parity][2 halves][128 rows]
+constexpr uint32_t kSmLsum = kSmMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]
+constexpr uint32_t kSmBar = kSmLsum + 2 * 128 * 4;
+
+enum : int {
+    Q_FULL = 0,                                    // [2]
+    Q_EMPTY = Q_FULL + 2,                          // [2]
+    K_FULL = Q_EMPTY + 2,
+    K_EMPTY = K_FULL + kKStages,
+    V_FULL = K_EMPTY + kKStages,
+    V_EMPTY = V_FULL + kVStages,
+    S_FULL = V_EMPTY + kVStages,
+    P_FULL = S_FULL + kSBufs,
+    PV_DONE = P_FULL + kSBufs,
+    O_FREE = PV_DONE + kSBufs,
+    DRAIN = O_FREE + 1,
+    NUM_BARS = DRAIN + 1
+};
+
+constexpr uint32_t kSmTmemSlot = kSmBar + NUM_BARS * 8;
+constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
+constexpr uint32_t kSmEpiSkip = kSmAbort + 4;
+constexpr uint32_t kSmUsed = kSmEpiSkip + 4;
+constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
+
+__device__ __forceinline__ uint32_t bar(uint32_t sbase, int i) { return sbase + kSmBar + 8u * i; }
+
+// One unit of work: sequence b, KV head kvh, query tile qt (this CTA's of the pair).
+struct Unit {
+    int b, kvh, n0, lo, L, n_pre, n_tiles;
+    bool ok;                                       // consistent prefix offsets
+};
+
+__device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, uint32_t crank) {
+    Unit u;
+    const int per_b = p.Hkv * pairs;
+    u.b = U / per_b;
+    const int r = U - u.b * per_b;
+    u.kvh = r / pairs;
+    const int pair = r - u.kvh * pairs;
+    u.n0 = (pair * kCluster + (int)crank) * p.tok_per_tile;
+    u.lo = __ldg(p.cu_prefix + u.b);
+    const int hi = __ldg(p.cu_prefix + u.b + 1);
+    u.L = hi - u.lo;
+    u.ok = !(u.lo < 0 || u.L < 0 || (int64_t)hi > p.total_prefix || u.L > p.max_prefix);
+    u.n_pre = (u.L + kBlockN - 1) / kBlockN;
+    u.n_tiles = u.ok ? u.n_pre + (p.N + kBlockN - 1) / kBlockN : 0;
+    return u;
+}
+
+}  // namespace pk
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                                const __grid_constant__ CUtensorMap tm_kimg,
+                                const __grid_constant__ CUtensorMap tm_vimg,
+                                const __grid_constant__ CUtensorMap tm_kpre,
+                                const __grid_constant__ CUtensorMap tm_vpre, const AttnParams p, int n_units,
+                                int pairs) {
+    using pk::bar;
+    using pk::decode;
+    using pk::Unit;
+    using pk::Q_FULL;
+    using pk::Q_EMPTY;
+    using pk::K_FULL;
+    using pk::K_EMPTY;
+    using pk::V_FULL;
+    using pk::V_EMPTY;
+    using pk::S_FULL;
+    using pk::P_FULL;
+    using pk::PV_DONE;
+    using pk::O_FREE;
+    using pk::DRAIN;
+    using pk::kSmQ0;
+    using pk::kQLead;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cid = blockIdx.x / kCluster;             // cluster index
+    const int ncl = gridDim.x / kCluster;
+
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pk::kSmAbort);
+    volatile int* epi_skip = reinterpret_cast<volatile int*>(smem + pk::kSmEpiSkip);
+    const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        *epi_skip = 0;
+        for (int i = 0; i < pk::NUM_BARS; ++i) {
+            uint32_t count = 1;
+            if ((i >= P_FULL && i < P_FULL + kSBufs) || i == O_FREE) count = kSoftmaxThreads;
+            if ((i >= K_EMPTY && i < K_EMPTY + pk::kKStages) || (i >= V_EMPTY && i < V_EMPTY + pk::kVStages))
+                count = kCluster;                // released by the MMA of every CTA of the cluster
+            if (i == DRAIN) count = 2;          // one commit from each MMA issuer
+            mbar_init(bar(sb, i), count);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + pk::kSmTmemSlot, kTmCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    // No CTA may multicast into a peer before the peer's barriers exist.
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + pk::kSmTmemSlot);
+    const uint32_t crank = cluster_ctarank();
+    if (threadIdx.x == 0) {
+        // Report inconsistent prefix offsets once per CTA; such units are skipped by every role.
+        for (int U = cid; U < n_units; U += ncl)
+            if (!decode(p, U, pairs, crank).ok) {
+                atomicOr(&g_dev_error, NEO_DEVERR_BAD_PREFIX);
+                break;
+            }
+    }
+
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers: Q and K (warp 0), V (warp 2)
+        if (lane == 0) {
+            const bool is_k = warp == 0;
+            const int stages = is_k ? pk::kKStages : pk::kVStages;
+            const int full0 = is_k ? K_FULL : V_FULL;
+            const int empty0 = is_k ? K_EMPTY : V_EMPTY;
+            const uint32_t ring = sb + (is_k ? pk::kSmK : pk::kSmV);
+            const CUtensorMap* pre_map = is_k ? &tm_kpre : &tm_vpre;
+            const CUtensorMap* img_map = is_k ? &tm_kimg : &tm_vimg;
+            bool ok = true;
+            int gt = 0, uq = 0, q_issued = -1;
+            // Q of the uq-th non-empty unit into buffer uq % 2, once the store of
+            // the unit that used that buffer before has read it.
+            auto issue_q = [&](const Unit& u, int uqi) -> bool {
+                const int buf = uqi & 1;
+                if (uqi >= 2 && !wait(bar(sb, Q_EMPTY + buf), (uint32_t)((uqi - 2) >> 1) & 1u)) return false;
+                const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
+                mbar_arrive_expect_tx(bar(sb, Q_FULL + buf), kTile);
+                tma_load_4d(sQ, &tm_q, bar(sb, Q_FULL + buf), 0, u.kvh * p.G, u.n0, u.b);
+                tma_load_4d(sQ + kHalfTile, &tm_q, bar(sb, Q_FULL + buf), 64, u.kvh * p.G, u.n0, u.b);
+                q_issued = uqi;
+                return true;
+            };
+            for (int U = cid; ok && U < n_units; U += ncl) {
+                const Unit u = decode(p, U, pairs, crank);
+                if (u.n_tiles == 0) continue;
+                if (is_k && uq == 0) ok = issue_q(u, 0);
+                for (int j = 0; ok && j < u.n_tiles; ++j) {
+                    const int st = gt % stages;
+                    if (!wait(bar(sb, empty0 + st), ((uint32_t)(gt / stages) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar(sb, full0 + st);
+                    const uint32_t dst = ring + (uint32_t)st * kTile;
+                    mbar_arrive_expect_tx(fb, kTile);
+                    const uint32_t hdst = dst + crank * kHalfTile;
+                    const int d0 = 64 * (int)crank;
+                    if (j < u.n_pre)
+                        tma_load_3d_mc(hdst, pre_map, fb, d0, u.kvh, u.lo + j * kBlockN, kClusterMask);
+                    else
+                        tma_load_4d_mc(hdst, img_map, fb, d0, u.kvh, (j - u.n_pre) * kBlockN, u.b, kClusterMask);
+                    ++gt;
+                    // The next unit's Q, kQLead tiles before this unit's last K tile
+                    // (after this tile's K: the softmax's release of the Q buffer
+                    // happens at tile min(1, jq) of a unit, which needs that K).
+                    if (is_k && j == max(0, u.n_tiles - kQLead)) {
+                        for (int U2 = U + ncl; U2 < n_units; U2 += ncl) {   // the next non-empty unit
+                            const Unit u2 = decode(p, U2, pairs, crank);
+                            if (u2.n_tiles > 0) {
+                                ok = issue_q(u2, uq + 1);
+                                break;
+                            }
+                        }
+                    }
+                }
+                ++uq;
+            }
+            if (*abort_flag) {
+                // Let copies already in flight land before the CTA's shared memory goes away.
+                if (is_k && q_issued >= 0) {
+                    wait(bar(sb, Q_FULL + (q_issued & 1)), (uint32_t)(q_issued >> 1) & 1u, false);
+                    if (q_issued >= 1)
+                        wait(bar(sb, Q_FULL + ((q_issued - 1) & 1)), (uint32_t)((q_issued - 1) >> 1) & 1u, false);
+                }
+                for (int g = (gt > stages ? gt - stages : 0); g < gt; ++g)
+                    wait(bar(sb, full0 + g % stages), (uint32_t)(g / stages) & 1u, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        if (lane == 0) {
+            bool ok = true;
+            int gt = 0, uq = 0;
+            for (int U = cid; ok && U < n_units; U += ncl) {
+                const Unit u = decode(p, U, pairs, crank);
+                if (u.n_tiles == 0) continue;
+                if (warp == 1) {
+                    const int buf = uq & 1;
+                    const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
+                    if (!wait(bar(sb, Q_FULL + buf), (uint32_t)(uq >> 1) & 1u)) break;
+                    tc_fence_after();
+                    for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                        const int st = gt % pk::kKStages;
+                        if (!wait(bar(sb, K_FULL + st), (uint32_t)(gt / pk::kKStages) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        // S buffer gt%3 holds P of tile gt-3 until that tile's PV has read it.
+                        const int sbuf = gt % kSBufs;
+                        if (gt >= kSBufs && !wait(bar(sb, PV_DONE + sbuf), ((uint32_t)(gt / kSBufs) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sK = sb + pk::kSmK + (uint32_t)st * kTile;
+                        const uint32_t d = tmem + kTmS0 + (uint32_t)sbuf * 128u;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                            mma_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
+                                   kIdescS, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(sb, S_FULL + sbuf));
+                        mma_commit_mc(bar(sb, K_EMPTY + st), kClusterMask);
+                    }
+                } else {
+                    // The unit's first PV overwrites O: the previous unit's epilogue must have read it.
+                    if (uq > 0 && !wait(bar(sb, O_FREE), (uint32_t)(uq - 1) & 1u)) break;
+                    for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                        const int st = gt % pk::kVStages;
+                        const int sbuf = gt % kSBufs;
+                        if (!wait(bar(sb, P_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u) ||
+                            !wait(bar(sb, V_FULL + st), (uint32_t)(gt / pk::kVStages) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sV = sb + pk::kSmV + (uint32_t)st * kTile;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            mma_ts(tmem + kTmO, tmem + kTmS0 + (uint32_t)sbuf * 128u + (uint32_t)kk * 8u,
+                                   smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(bar(sb, PV_DONE + sbuf));
+                        mma_commit_mc(bar(sb, V_EMPTY + st), kClusterMask);
+                    }
+                }
+                ++uq;
+            }
+            // Drain: every MMA issued above completes before TMEM is released.
+            mma_commit(bar(sb, DRAIN));
+            wait(bar(sb, DRAIN), 0, false);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int half = (warp - 4) >> 2;          // key columns [64*half, 64*half + 64)
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t pair_bar = 2u + (uint32_t)quad;   // the two warps sharing these TMEM lanes
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        float* mx_s = reinterpret_cast<float*>(smem + pk::kSmMax);
+        float* ls_s = reinterpret_cast<float*>(smem + pk::kSmLsum);
+        bool failed = false;
+        int gt = 0, uq = 0;
+        // The epilogue of a unit. Every softmax thread reaches it after the unit's
+        // tiles, failed or not, so that all of them meet at its barriers.
+        struct Pending {
+            int b, kvh, n0, buf, last_gt;
+            float m_used, l_part;
+        };
+        auto epilogue = [&](const Pending& e) {
+            // Only these eight warps write epi_skip, and only before the first
+            // barrier below, so after it every warp of the group takes the same branch.
+            bool ok = !failed;
+            if (ok)
+                ok = __all_sync(0xffffffffu, wait(bar(sb, PV_DONE + e.last_gt % kSBufs),
+                                                  (uint32_t)(e.last_gt / kSBufs) & 1u));
+            if (!ok) {
+                failed = true;
+                *epi_skip = 1;
+            }
+            ls_s[half * 128 + row] = e.l_part;
+            named_barrier_sync(1, kSoftmaxThreads);
+            if (*epi_skip) return;
+            tc_fence_after();
+            const float l_sum = ls_s[row] + ls_s[128 + row];
+            const float inv_l = 1.0f / l_sum;
+            uint32_t r[2][32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u, r[c]);
+            // O is read: the next unit's first PV may overwrite it.
+            tc_fence_before();
+            mbar_arrive(bar(sb, O_FREE));
+            // The unit's Q buffer (its last S has completed) stages the output.
+            uint8_t* stage = smem + kSmQ0 + (uint32_t)e.buf * kTile + (uint32_t)half * kHalfTile;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(r[c][qd * 8 + 0]) * inv_l, __uint_as_float(r[c][qd * 8 + 1]) * inv_l);
+                    v.y = pack_bf16x2(__uint_as_float(r[c][qd * 8 + 2]) * inv_l, __uint_as_float(r[c][qd * 8 + 3]) * inv_l);
+                    v.z = pack_bf16x2(__uint_as_float(r[c][qd * 8 + 4]) * inv_l, __uint_as_float(r[c][qd * 8 + 5]) * inv_l);
+                    v.w = pack_bf16x2(__uint_as_float(r[c][qd * 8 + 6]) * inv_l, __uint_as_float(r[c][qd * 8 + 7]) * inv_l);
+                    const int chunk = c * 4 + qd;
+                    const uint32_t off = (uint32_t)row * 128u + (uint32_t)((chunk ^ (row & 7)) << 4);
+                    *reinterpret_cast<uint4*>(stage + off) = v;
+                }
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(1, kSoftmaxThreads);
+            if (threadIdx.x == 4 * 32) {
+                if (e.n0 < p.N) {
+                    const uint32_t sQ = sb + kSmQ0 + (uint32_t)e.buf * kTile;
+                    tma_store_4d(&tm_o, sQ, 0, e.kvh * p.G, e.n0, e.b);
+                    tma_store_4d(&tm_o, sQ + kHalfTile, 64, e.kvh * p.G, e.n0, e.b);
+                    tma_store_commit_and_wait_read();
+                }
+                mbar_arrive(bar(sb, Q_EMPTY + e.buf));   // the buffer may take a later unit's Q
+            }
+            const int n = e.n0 + row / p.G;
+            if (half == 0 && p.lse != nullptr && n < p.N) {
+                const int h = e.kvh * p.G + row % p.G;
+                p.lse[((int64_t)e.b * p.Hq + h) * p.N + n] = (e.m_used + log2f(l_sum)) * 0.69314718055994531f;
+            }
+        };
+        for (int U = cid; U < n_units; U += ncl) {
+            const Unit u = decode(p, U, pairs, crank);
+            if (u.n_tiles == 0) continue;
+            const int buf = uq & 1;
+            float m_used = -INFINITY;
+            float l_part = 0.f;
+            // A failed wait sets `failed`: the loops then keep running without
+            // touching TMEM or the pipeline barriers, so that the two warps of a
+            // row pair still meet at every pair barrier.
+            for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                const int sbuf = gt % kSBufs;
+                const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
+                bool ok = !failed && __all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u));
+                float s[64];
+                float pmax = -INFINITY;
+                const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN)
+                                                   : min(kBlockN, p.N - (j - u.n_pre) * kBlockN);
+                const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
+                const bool masked = valid < 64;              // the same for the whole warp
+                float* mx_tile = mx_s + (gt & 1) * 256;
+                if (ok) {
+                    tc_fence_after();
+                    {
+                        uint32_t r[64];
+                        tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+                    }
+                    // Keys past the end of the prefix or image segment do not exist.
+                    if (masked) {
+                        // An opaque statement keeps this block behind its branch: the
+                        // compiler would otherwise turn it into selects run on every tile.
+                        asm volatile("");
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                    }
+                    // Partial row maximum of the raw logits (three-input max tree).
+                    float t1[22];
+#pragma unroll
+                    for (int i = 0; i < 21; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+                    t1[21] = s[63];
+                    float t2[8];
+#pragma unroll
+                    for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+                    t2[7] = t1[21];
+                    pmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
+                    mx_tile[half * 128 + row] = pmax;
+                }
+                // The other half's maximum comes through shared memory; both warps of
+                // the pair leave this barrier with the same verdict, and both have read
+                // all of S into registers, so either may then overwrite it with P.
+                tc_fence_before();
+                ok = named_barrier_and(pair_bar, 64, ok);
+                failed = !ok;
+                if (failed) continue;
+                tc_fence_after();
+                const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
+                const float m_new = fmaxf(m_used, mraw * p.scale_log2);
+                const bool need = m_new > m_used + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                    if (need) m_used = m_new;
+                    l_part *= alpha;
+                    if (j > 0) {
+                        failed = !__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + (gt - 1) % kSBufs),
+                                                               (uint32_t)((gt - 1) / kSBufs) & 1u));
+                        if (failed) continue;
+                        tc_fence_after();
+                        uint32_t r[32];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const uint32_t ocol = lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u;
+                            tmem_ld32(ocol, r);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(ocol, r);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                // p = 2^(s*scale*log2e - m): a hidden key's -inf logit stays -inf
+                // (the scale is > 0 and m finite from the first tile on), so its p is 0.
+                const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nm = make_float2(-m_used, -m_used);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
+                    const float2 e = make_float2(ex2(a.x), ex2(a.y));
+                    acc[c & 3] = fadd2(acc[c & 3], e);
+                    pk[c] = pack_bf16x2(e.x, e.y);
+                }
+                l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                          ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+                tmem_st32(lane_base + scol + (uint32_t)half * 32u, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(sb, P_FULL + sbuf));
+            }
+            epilogue(Pending{u.b, u.kvh, u.n0, buf, gt - 1, m_used, l_part});
+            ++uq;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // The peer may still multicast into this CTA's shared memory or arrive on its
+    // barriers until it is done as well.
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmCols);
+    }
+}
+
 // --------------------------------------------------------------------- host
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -853,6 +1329,9 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         for (const void* k : kernels)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(gen_attention_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)pk::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
 
@@ -883,8 +1362,39 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     // Query tiles come in clusters of kCluster (a tile past the last token loads,
     // computes and stores nothing of its own but still shares the K/V stream).
     const int qtiles = (N + tok_per_tile - 1) / tok_per_tile;
-    const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
     const bool bc = mask_mode == NEO_MASK_BLOCK_CAUSAL;
+    if (!bc && !qn) {
+        // Full mask: the persistent kernel, one cluster per pair of SMs it can
+        // keep resident, each working through its share of the units.
+        static std::once_flag occ_once;
+        static int max_clusters = 0;
+        std::call_once(occ_once, [] {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = kCluster;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(kCluster * 1024, 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = pk::kSmemBytes;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void*)gen_attention_persistent_kernel, &cfg) !=
+                cudaSuccess)
+                max_clusters = 0;
+            cudaGetLastError();
+        });
+        if (max_clusters < 1) return NEO_ERR_CUDA;
+        const int pairs = (qtiles + kCluster - 1) / kCluster;
+        const int64_t n_units = (int64_t)B * Hkv * pairs;
+        if (n_units > 0x7fffffffLL) return NEO_ERR_UNSUPPORTED;
+        const int clusters = (int)std::min<int64_t>(n_units, max_clusters);
+        gen_attention_persistent_kernel<<<dim3((unsigned)(clusters * kCluster)), kThreads, pk::kSmemBytes, stream>>>(
+            tq, to, tki, tvi, tkp, tvp, prm, (int)n_units, pairs);
+        return neo::launch_status();
+    }
+    const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
     auto kernel = bc ? (qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>)
                      : (qn ? gen_attention_kernel<false, true> : gen_attention_kernel<false, false>);
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, fr, prm);

@@ -1205,6 +1205,24 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     }
 }
 
+// --------------------------------------------------------------------- wait self-test
+// One thread waits, with the kernels' bounded wait, on an mbarrier that
+// nothing arrives at. The wait gives up after the configured limit, raises the
+// abort flag and records NEO_DEVERR_TIMEOUT, exactly as a stalled pipeline
+// wait inside the attention kernels does; there are no copies, MMAs or TMEM
+// to unwind, so the test leaves the context as it found it.
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel() {
+    __shared__ __align__(8) uint64_t barrier;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    const uint32_t b = smem_addr(&barrier);
+    mbar_init(b, 1);
+    fence_barrier_init();
+    const BoundedWait wait{&abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
+    wait(b, 0);   // phase 0 never completes
+}
+
 // --------------------------------------------------------------------- host
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1423,4 +1441,9 @@ extern "C" neo_status neo_gen_attention_qnorm(const void* q_img_raw, const void*
     if (!qnorm) return NEO_ERR_INVALID_ARG;
     return launch_attention(q_img_raw, k_prefix, v_prefix, k_img, v_img, dtype, cu_prefix, total_prefix, max_prefix,
                             B, N, Hq, Hkv, D, mask_mode, t_prefix, t_img, qnorm, scale, out, lse, stream);
+}
+
+extern "C" neo_status neo_selftest_bounded_wait(cudaStream_t stream) {
+    bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>();
+    return neo::launch_status();
 }

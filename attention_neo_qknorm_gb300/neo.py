@@ -29,7 +29,8 @@ EXPORTS = ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_
            "neo_write_prefix_cache", "neo_flow_euler_step",
            "neo_flow_cfg_euler_step", "neo_time_schedule", "neo_noise_scale", "neo_scale_noise",
            "neo_rope2d_interleaved",
-           "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_version")
+           "neo_status_string", "neo_get_device_error", "neo_set_wait_timeout_ns", "neo_selftest_bounded_wait",
+           "neo_version")
 
 
 class NeoError(RuntimeError):
@@ -82,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.neo_status_string.restype = ctypes.c_char_p
     lib.neo_get_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.neo_set_wait_timeout_ns.argtypes = [_u64]
+    lib.neo_selftest_bounded_wait.argtypes = [_vp]
     lib.neo_version.argtypes = []
     for name in ("neo_build_positions", "neo_qknorm_rope3", "neo_gen_attention", "neo_flow_euler_step",
                  "neo_flow_cfg_euler_step", "neo_time_schedule", "neo_noise_scale", "neo_scale_noise",
@@ -299,6 +301,11 @@ def neo_get_device_error(stream=None) -> tuple[int, int]:
 
 def neo_set_wait_timeout_ns(ns: int):
     _check(load_library().neo_set_wait_timeout_ns(int(ns)), "neo_set_wait_timeout_ns")
+
+
+def neo_selftest_bounded_wait(stream=None):
+    """Enqueue the bounded-wait self-test (a wait that runs out; see neo.h)."""
+    _check(load_library().neo_selftest_bounded_wait(_stream(stream)), "neo_selftest_bounded_wait")
 
 
 def neo_version() -> int:

@@ -338,6 +338,13 @@ neo_status neo_get_device_error(cudaStream_t stream, uint32_t* word);
  * nanoseconds (default 1e9). Applies to launches enqueued afterwards. */
 neo_status neo_set_wait_timeout_ns(uint64_t ns);
 
+/* Self-test of the kernels' bounded waits: one thread waits on a barrier
+ * that nothing arrives at; after the limit set by neo_set_wait_timeout_ns the
+ * wait gives up and records NEO_DEVERR_TIMEOUT, which the next
+ * neo_get_device_error returns as NEO_ERR_TIMEOUT. Nothing else is touched,
+ * so the context stays usable. */
+neo_status neo_selftest_bounded_wait(cudaStream_t stream);
+
 /* ABI version of this header (major * 100 + minor). */
 int neo_version(void);
 

@@ -208,3 +208,23 @@ def test_block_causal_full_size_prefill_sampled_rows(gpu_lib, chunk):
     got = f64(out.cpu())[0, rows[:, 1], rows[:, 2]]
     assert_bf16_close(got, ref, f"block-causal prefill chunk={chunk}")
     np.testing.assert_allclose(f64(lse.cpu())[0, rows[:, 2], rows[:, 1]], ref_lse, rtol=1e-4, atol=1e-3)
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable(gpu_lib):
+    """A wait on a barrier that nothing arrives at gives up after the
+    configured limit and reports NEO_ERR_TIMEOUT; attention still runs
+    correctly afterwards."""
+    import time
+    neo.neo_get_device_error()          # clear
+    neo.neo_set_wait_timeout_ns(20_000_000)   # 20 ms
+    try:
+        t0 = time.perf_counter()
+        neo.neo_selftest_bounded_wait()
+        st, word = neo.neo_get_device_error()
+        elapsed = time.perf_counter() - t0
+    finally:
+        neo.neo_set_wait_timeout_ns(1_000_000_000)
+    assert st == neo.NEO_ERR_TIMEOUT and word & neo.NEO_DEVERR_TIMEOUT
+    assert elapsed < 5.0
+    run_case((200, 77), 132, 8, 2, seed=3)
+    assert neo.neo_get_device_error() == (neo.NEO_OK, 0)

@@ -1340,8 +1340,8 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        const void* kernels[4] = {(const void*)gen_attention_kernel<false, false>,
-                                  (const void*)gen_attention_kernel<true, false>,
+        // (the full mask without the folded norm runs in the persistent kernel)
+        const void* kernels[3] = {(const void*)gen_attention_kernel<true, false>,
                                   (const void*)gen_attention_kernel<false, true>,
                                   (const void*)gen_attention_kernel<true, true>};
         for (const void* k : kernels)
@@ -1414,7 +1414,7 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     }
     const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
     auto kernel = bc ? (qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>)
-                     : (qn ? gen_attention_kernel<false, true> : gen_attention_kernel<false, false>);
+                     : gen_attention_kernel<false, true>;
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, fr, prm);
     return neo::launch_status();
 }

@@ -228,3 +228,14 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable(gpu_lib):
     assert elapsed < 5.0
     run_case((200, 77), 132, 8, 2, seed=3)
     assert neo.neo_get_device_error() == (neo.NEO_OK, 0)
+
+
+def test_many_short_units_per_cluster(gpu_lib):
+    """300 sequences with short ragged prefixes and 40 image tokens each: the
+    persistent kernel then runs several one- or two-tile units per cluster
+    back to back (next query loaded at a unit's first tile, buffers released
+    between tiny units)."""
+    rng = np.random.default_rng(12)
+    prefix = tuple(int(x) for x in rng.integers(0, 120, size=300))
+    out = run_case(prefix, 40, 4, 1, seed=13)
+    assert torch.isfinite(out).all()

@@ -205,3 +205,20 @@ def test_rope2d_interleaved_matches_oracle(gpu_lib, dtype, n_img, rows, cols, C)
         assert_bf16_close(f64(xd), ref, "rope2d bf16")
     else:
         assert max_abs(f64(xd), ref) < 2e-5
+
+
+def test_cfg_euler_full_size_dual(gpu_lib):
+    """The configuration the bench times beside the step: dual guidance on the
+    2048^2 workload's 4096 x 3072 fp32 patches with three predictions."""
+    w = synth.WORKLOADS["gen_2048"]
+    z, xs = synth.make_flow(w, n_x0=3)
+    zd, vd = z.cuda(), torch.empty_like(z, device="cuda")
+    branch = neo.neo_flow_cfg_euler_step(zd, xs[0].cuda(), xs[1].cuda(), xs[2].cuda(), 0.5, 0.55, 4.0, 1.5,
+                                         v_out=vd)
+    f32 = np.float32
+    rz, rv, rb = O.flow_cfg_euler_step(f64(z), f64(xs[0]), f64(xs[1]), f64(xs[2]), f32(0.5), f32(0.55), f32(4.0),
+                                       f32(1.5), (f32(0.0), f32(1.0)), t_eps=f32(0.02))
+    assert branch == rb == neo.NEO_CFG_DUAL
+    for got, ref in ((f64(zd), rz), (f64(vd), rv)):
+        assert rel_frob(got, ref) <= F32_TOL
+        assert max_abs(got, ref) <= F32_TOL * max(1.0, float(np.abs(ref).max()))

@@ -131,3 +131,14 @@ def test_chunked_prefill_through_the_cache(gpu_lib):
                               t_prefix=np.zeros(0, np.int32), t_img=T[:, :c])
     assert_bf16_close(f64(out1.cpu()), ref1, "chunk 1")
     assert_bf16_close(f64(out2.cpu()), ref[:, c:], "chunk 2 through the cache")
+
+
+def test_cache_write_bench_shape(gpu_lib):
+    """The append the bench times: caches of 300 / 777 / 1500 / 2048 rows plus
+    512-token chunks, 8 KV heads, bf16 (54.7 MB moved)."""
+    k_old, v_old, cu, k_new, v_new, n, cap = _case((300, 777, 1500, 2048), 512, (512, 512, 512, 512), Hkv=8,
+                                                   seed=21, extra=0)
+    k, v, cu_out = _run(k_old, v_old, cu, k_new, v_new, n, cap)
+    rk, rv, rcu = O.write_prefix_cache(f64(k_old), f64(v_old), cu, f64(k_new), f64(v_new), n)
+    assert np.array_equal(cu_out, rcu)
+    assert np.array_equal(f64(k), rk) and np.array_equal(f64(v), rv)

@@ -8,6 +8,14 @@
 // applies the block-causal mask of the mixed prefill (section "Block-causal
 // attention"): key j visible to query i iff T_j == T_i or j <= i.
 //
+// Two kernels share the roles below. gen_attention_persistent_kernel (the
+// full mask without the folded query norm) keeps one cluster per pair of SMs
+// resident and walks it through a sequence of query-tile pairs, so one
+// pair's epilogue overlaps the next pair's first tiles (its own comment,
+// further down, gives the hand-over). gen_attention_kernel (block-causal
+// mask and/or the query norm folded into the prologue) runs one query tile
+// per CTA.
+//
 // Kernel shape (one CTA per 128-row query tile; D = 128; 12 warps; clusters
 // of two CTAs):
 //   * A query tile packs the G = Hq/Hkv heads of one KV group for 128/G
@@ -740,10 +748,20 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 // unit's first tiles overlap:
 //   * Q is double-buffered. The next unit's Q is loaded kQLead tiles before
 //     the current unit's last K tile; a unit's Q buffer becomes the staging
-//     buffer of its output once its last S has completed, and is refilled
-//     only after that output's store has read it (Q_EMPTY).
-//   * The next unit's first PV overwrites O only after every softmax thread
-//     has read the finished O (O_FREE).
+//     buffer of its output once its last S has completed.
+//   * The softmax threads' part of the epilogue is short: the row pair's
+//     partial sums are combined (one pair barrier), the LSE is written, then
+//     O is read from TMEM (O_FREE: the next unit's first PV may overwrite it),
+//     normalised and staged; each thread then arrives on STAGED and goes on
+//     to the next unit. The Q/K producer lane issues the staged tile's TMA
+//     store when it sees STAGED complete (polled between its K loads) and
+//     waits for the store's shared-memory read only before it loads a later
+//     unit's Q into that buffer.
+//   * Every role decodes the unit after the one it is working on in advance,
+//     so the prefix offsets' global loads are off the unit boundary.
+//   * The S issuer holds a unit's second S until the previous unit's last PV
+//     has completed, so that PV, which the epilogue waits for, is not queued
+//     behind two S batches of the next unit.
 //   * K and V rings, S buffers and the pair exchange run on one tile counter
 //     across units. K has two stages here to make room for the second Q.
 // The softmax of a tile is the same as in gen_attention_kernel.
@@ -762,8 +780,8 @@ constexpr uint32_t kSmBar = kSmLsum + 2 * 128 * 4;
 
 enum : int {
     Q_FULL = 0,                                    // [2]
-    Q_EMPTY = Q_FULL + 2,                          // [2]
-    K_FULL = Q_EMPTY + 2,
+    STAGED = Q_FULL + 2,                           // [2] a unit's output is in its Q buffer
+    K_FULL = STAGED + 2,
     K_EMPTY = K_FULL + kKStages,
     V_FULL = K_EMPTY + kKStages,
     V_EMPTY = V_FULL + kVStages,
@@ -777,8 +795,7 @@ enum : int {
 
 constexpr uint32_t kSmTmemSlot = kSmBar + NUM_BARS * 8;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
-constexpr uint32_t kSmEpiSkip = kSmAbort + 4;
-constexpr uint32_t kSmUsed = kSmEpiSkip + 4;
+constexpr uint32_t kSmUsed = kSmAbort + 4;
 constexpr uint32_t kSmemBytes = kSmUsed + 1024;    // slack to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 
@@ -790,21 +807,44 @@ struct Unit {
     bool ok;                                       // consistent prefix offsets
 };
 
-__device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, uint32_t crank) {
+// The prefix offsets of unit U's sequence. Every role loads them a unit
+// ahead: the loads are issued when a unit starts and their values are first
+// used (finish_unit) when it ends, so that their latency is not spent at the
+// unit boundary.
+struct UnitLoad {
+    int U, lo, hi;
+};
+
+__device__ __forceinline__ int ld_nc_s32(const int* ptr) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ UnitLoad load_unit(const AttnParams& p, int U, int pairs) {
+    const int b = U / (p.Hkv * pairs);
+    return UnitLoad{U, ld_nc_s32(p.cu_prefix + b), ld_nc_s32(p.cu_prefix + b + 1)};
+}
+
+__device__ __forceinline__ Unit finish_unit(const AttnParams& p, const UnitLoad& l, int pairs, uint32_t crank) {
     Unit u;
     const int per_b = p.Hkv * pairs;
-    u.b = U / per_b;
-    const int r = U - u.b * per_b;
+    u.b = l.U / per_b;
+    const int r = l.U - u.b * per_b;
     u.kvh = r / pairs;
     const int pair = r - u.kvh * pairs;
     u.n0 = (pair * kCluster + (int)crank) * p.tok_per_tile;
-    u.lo = __ldg(p.cu_prefix + u.b);
-    const int hi = __ldg(p.cu_prefix + u.b + 1);
+    u.lo = l.lo;
+    const int hi = l.hi;
     u.L = hi - u.lo;
     u.ok = !(u.lo < 0 || u.L < 0 || (int64_t)hi > p.total_prefix || u.L > p.max_prefix);
     u.n_pre = (u.L + kBlockN - 1) / kBlockN;
     u.n_tiles = u.ok ? u.n_pre + (p.N + kBlockN - 1) / kBlockN : 0;
     return u;
+}
+
+__device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, uint32_t crank) {
+    return finish_unit(p, load_unit(p, U, pairs), pairs, crank);
 }
 
 }  // namespace pk
@@ -818,9 +858,12 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                                 int pairs) {
     using pk::bar;
     using pk::decode;
+    using pk::finish_unit;
+    using pk::load_unit;
+    using pk::UnitLoad;
     using pk::Unit;
     using pk::Q_FULL;
-    using pk::Q_EMPTY;
+    using pk::STAGED;
     using pk::K_FULL;
     using pk::K_EMPTY;
     using pk::V_FULL;
@@ -841,15 +884,14 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     const int ncl = gridDim.x / kCluster;
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pk::kSmAbort);
-    volatile int* epi_skip = reinterpret_cast<volatile int*>(smem + pk::kSmEpiSkip);
     const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        *epi_skip = 0;
         for (int i = 0; i < pk::NUM_BARS; ++i) {
             uint32_t count = 1;
-            if ((i >= P_FULL && i < P_FULL + kSBufs) || i == O_FREE) count = kSoftmaxThreads;
+            if ((i >= P_FULL && i < P_FULL + kSBufs) || i == O_FREE || (i >= STAGED && i < STAGED + 2))
+                count = kSoftmaxThreads;
             if ((i >= K_EMPTY && i < K_EMPTY + pk::kKStages) || (i >= V_EMPTY && i < V_EMPTY + pk::kVStages))
                 count = kCluster;                // released by the MMA of every CTA of the cluster
             if (i == DRAIN) count = 2;          // one commit from each MMA issuer
@@ -878,7 +920,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     }
 
     if (warp == 0 || warp == 2) {
-        // ------------------------------------------------------------ producers: Q and K (warp 0), V (warp 2)
+        // ------------------------------------------------------------ producers: Q, K and the output stores (warp 0), V (warp 2)
         if (lane == 0) {
             const bool is_k = warp == 0;
             const int stages = is_k ? pk::kKStages : pk::kVStages;
@@ -889,52 +931,88 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             const CUtensorMap* img_map = is_k ? &tm_kimg : &tm_vimg;
             bool ok = true;
             int gt = 0, uq = 0, q_issued = -1;
-            // Q of the uq-th non-empty unit into buffer uq % 2, once the store of
-            // the unit that used that buffer before has read it.
+            // Output stores. st_next: the first non-empty unit whose output has not
+            // been stored; qc0 / qc1: head, token and sequence coordinates of the
+            // unit whose Q (and then output) is in buffer 0 / 1.
+            int st_next = 0;
+            int3 qc0 = make_int3(0, 0, 0), qc1 = make_int3(0, 0, 0);
+            // The TMA store of unit st_next's output once the softmax threads have
+            // staged it; without `block` only if they already have.
+            auto store_next = [&](bool block) -> bool {
+                const int buf = st_next & 1;
+                const uint32_t sbar = bar(sb, STAGED + buf);
+                const uint32_t par = (uint32_t)(st_next >> 1) & 1u;
+                if (block ? !wait(sbar, par) : !mbar_try_wait(sbar, par)) return false;
+                const int3 c = buf ? qc1 : qc0;
+                if (c.y < p.N) {
+                    const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
+                    tma_store_4d(&tm_o, sQ, 0, c.x, c.y, c.z);
+                    tma_store_4d(&tm_o, sQ + kHalfTile, 64, c.x, c.y, c.z);
+                    tma_store_commit();
+                }
+                ++st_next;
+                return true;
+            };
+            // Q of the uq-th non-empty unit into buffer uq % 2, once the output of
+            // the unit that used that buffer before has been stored and read.
             auto issue_q = [&](const Unit& u, int uqi) -> bool {
                 const int buf = uqi & 1;
-                if (uqi >= 2 && !wait(bar(sb, Q_EMPTY + buf), (uint32_t)((uqi - 2) >> 1) & 1u)) return false;
+                if (uqi >= 2) {
+                    while (st_next <= uqi - 2)
+                        if (!store_next(true)) return false;
+                    tma_store_wait_read();
+                }
                 const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
                 mbar_arrive_expect_tx(bar(sb, Q_FULL + buf), kTile);
                 tma_load_4d(sQ, &tm_q, bar(sb, Q_FULL + buf), 0, u.kvh * p.G, u.n0, u.b);
                 tma_load_4d(sQ + kHalfTile, &tm_q, bar(sb, Q_FULL + buf), 64, u.kvh * p.G, u.n0, u.b);
+                (buf ? qc1 : qc0) = make_int3(u.kvh * p.G, u.n0, u.b);
                 q_issued = uqi;
                 return true;
             };
+            Unit nxt = cid < n_units ? decode(p, cid, pairs, crank) : Unit{};
             for (int U = cid; ok && U < n_units; U += ncl) {
-                const Unit u = decode(p, U, pairs, crank);
-                if (u.n_tiles == 0) continue;
-                if (is_k && uq == 0) ok = issue_q(u, 0);
-                for (int j = 0; ok && j < u.n_tiles; ++j) {
-                    const int st = gt % stages;
-                    if (!wait(bar(sb, empty0 + st), ((uint32_t)(gt / stages) & 1u) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar(sb, full0 + st);
-                    const uint32_t dst = ring + (uint32_t)st * kTile;
-                    mbar_arrive_expect_tx(fb, kTile);
-                    const uint32_t hdst = dst + crank * kHalfTile;
-                    const int d0 = 64 * (int)crank;
-                    if (j < u.n_pre)
-                        tma_load_3d_mc(hdst, pre_map, fb, d0, u.kvh, u.lo + j * kBlockN, kClusterMask);
-                    else
-                        tma_load_4d_mc(hdst, img_map, fb, d0, u.kvh, (j - u.n_pre) * kBlockN, u.b, kClusterMask);
-                    ++gt;
-                    // The next unit's Q, kQLead tiles before this unit's last K tile
-                    // (after this tile's K: the softmax's release of the Q buffer
-                    // happens at tile min(1, jq) of a unit, which needs that K).
-                    if (is_k && j == max(0, u.n_tiles - kQLead)) {
-                        for (int U2 = U + ncl; U2 < n_units; U2 += ncl) {   // the next non-empty unit
-                            const Unit u2 = decode(p, U2, pairs, crank);
-                            if (u2.n_tiles > 0) {
-                                ok = issue_q(u2, uq + 1);
-                                break;
-                            }
+                const Unit u = nxt;
+                const bool more = U + ncl < n_units;
+                const UnitLoad ahead = more ? load_unit(p, U + ncl, pairs) : UnitLoad{0, 0, 0};
+                if (u.n_tiles > 0) {
+                    if (is_k && uq == 0) ok = issue_q(u, 0);
+                    for (int j = 0; ok && j < u.n_tiles; ++j) {
+                        const int st = gt % stages;
+                        if (!wait(bar(sb, empty0 + st), ((uint32_t)(gt / stages) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = bar(sb, full0 + st);
+                        const uint32_t dst = ring + (uint32_t)st * kTile;
+                        mbar_arrive_expect_tx(fb, kTile);
+                        const uint32_t hdst = dst + crank * kHalfTile;
+                        const int d0 = 64 * (int)crank;
+                        if (j < u.n_pre)
+                            tma_load_3d_mc(hdst, pre_map, fb, d0, u.kvh, u.lo + j * kBlockN, kClusterMask);
+                        else
+                            tma_load_4d_mc(hdst, img_map, fb, d0, u.kvh, (j - u.n_pre) * kBlockN, u.b, kClusterMask);
+                        ++gt;
+                        if (is_k && st_next < uq) store_next(false);
+                        // The next unit's Q, kQLead tiles before this unit's last K tile.
+                        // Its buffer holds the output of the unit before this one, whose
+                        // epilogue needs none of this unit's loads.
+                        if (is_k && more && j == max(0, u.n_tiles - kQLead)) {
+                            // The next non-empty unit (empty ones come only from bad prefix offsets).
+                            Unit u2 = finish_unit(p, ahead, pairs, crank);
+                            for (int U2 = U + 2 * ncl; u2.n_tiles == 0 && U2 < n_units; U2 += ncl)
+                                u2 = decode(p, U2, pairs, crank);
+                            if (u2.n_tiles > 0) ok = issue_q(u2, uq + 1);
                         }
                     }
+                    ++uq;
                 }
-                ++uq;
+                if (more) nxt = finish_unit(p, ahead, pairs, crank);
+            }
+            if (is_k) {
+                // The outputs of the last units; then every store has read its tile.
+                while (ok && st_next < uq) ok = store_next(true);
+                tma_store_wait_read();
             }
             if (*abort_flag) {
                 // Let copies already in flight land before the CTA's shared memory goes away.
@@ -953,62 +1031,73 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         if (lane == 0) {
             bool ok = true;
             int gt = 0, uq = 0;
+            Unit nxt = cid < n_units ? decode(p, cid, pairs, crank) : Unit{};
             for (int U = cid; ok && U < n_units; U += ncl) {
-                const Unit u = decode(p, U, pairs, crank);
-                if (u.n_tiles == 0) continue;
-                if (warp == 1) {
-                    const int buf = uq & 1;
-                    const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
-                    if (!wait(bar(sb, Q_FULL + buf), (uint32_t)(uq >> 1) & 1u)) break;
-                    tc_fence_after();
-                    for (int j = 0; j < u.n_tiles; ++j, ++gt) {
-                        const int st = gt % pk::kKStages;
-                        if (!wait(bar(sb, K_FULL + st), (uint32_t)(gt / pk::kKStages) & 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        // S buffer gt%3 holds P of tile gt-3 until that tile's PV has read it.
-                        const int sbuf = gt % kSBufs;
-                        if (gt >= kSBufs && !wait(bar(sb, PV_DONE + sbuf), ((uint32_t)(gt / kSBufs) & 1u) ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
+                const Unit u = nxt;
+                const bool more = U + ncl < n_units;
+                const UnitLoad ahead = more ? load_unit(p, U + ncl, pairs) : UnitLoad{0, 0, 0};
+                if (u.n_tiles > 0) {
+                    if (warp == 1) {
+                        const int buf = uq & 1;
+                        const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
+                        if (!wait(bar(sb, Q_FULL + buf), (uint32_t)(uq >> 1) & 1u)) break;
                         tc_fence_after();
-                        const uint32_t sK = sb + pk::kSmK + (uint32_t)st * kTile;
-                        const uint32_t d = tmem + kTmS0 + (uint32_t)sbuf * 128u;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-                            mma_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
-                                   kIdescS, kk > 0 ? 1u : 0u);
+                        for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                            const int st = gt % pk::kKStages;
+                            if (!wait(bar(sb, K_FULL + st), (uint32_t)(gt / pk::kKStages) & 1u)) {
+                                ok = false;
+                                break;
+                            }
+                            // S buffer gt%3 holds P of tile gt-3 until that tile's PV has read it.
+                            const int sbuf = gt % kSBufs;
+                            if (gt >= kSBufs && !wait(bar(sb, PV_DONE + sbuf), ((uint32_t)(gt / kSBufs) & 1u) ^ 1u)) {
+                                ok = false;
+                                break;
+                            }
+                            // The previous unit's last PV (tile gt-2) goes ahead of this unit's second S.
+                            if (j == 1 && uq > 0 &&
+                                !wait(bar(sb, PV_DONE + (gt - 2) % kSBufs), (uint32_t)((gt - 2) / kSBufs) & 1u)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sK = sb + pk::kSmK + (uint32_t)st * kTile;
+                            const uint32_t d = tmem + kTmS0 + (uint32_t)sbuf * 128u;
+    #pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                                mma_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
+                                       kIdescS, kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(bar(sb, S_FULL + sbuf));
+                            mma_commit_mc(bar(sb, K_EMPTY + st), kClusterMask);
                         }
-                        mma_commit(bar(sb, S_FULL + sbuf));
-                        mma_commit_mc(bar(sb, K_EMPTY + st), kClusterMask);
+                    } else {
+                        // The unit's first PV overwrites O: the previous unit's epilogue must have read it.
+                        if (uq > 0 && !wait(bar(sb, O_FREE), (uint32_t)(uq - 1) & 1u)) break;
+                        for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                            const int st = gt % pk::kVStages;
+                            const int sbuf = gt % kSBufs;
+                            if (!wait(bar(sb, P_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u) ||
+                                !wait(bar(sb, V_FULL + st), (uint32_t)(gt / pk::kVStages) & 1u)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sV = sb + pk::kSmV + (uint32_t)st * kTile;
+    #pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                mma_ts(tmem + kTmO, tmem + kTmS0 + (uint32_t)sbuf * 128u + (uint32_t)kk * 8u,
+                                       smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            mma_commit(bar(sb, PV_DONE + sbuf));
+                            mma_commit_mc(bar(sb, V_EMPTY + st), kClusterMask);
+                        }
                     }
-                } else {
-                    // The unit's first PV overwrites O: the previous unit's epilogue must have read it.
-                    if (uq > 0 && !wait(bar(sb, O_FREE), (uint32_t)(uq - 1) & 1u)) break;
-                    for (int j = 0; j < u.n_tiles; ++j, ++gt) {
-                        const int st = gt % pk::kVStages;
-                        const int sbuf = gt % kSBufs;
-                        if (!wait(bar(sb, P_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u) ||
-                            !wait(bar(sb, V_FULL + st), (uint32_t)(gt / pk::kVStages) & 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sV = sb + pk::kSmV + (uint32_t)st * kTile;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            mma_ts(tmem + kTmO, tmem + kTmS0 + (uint32_t)sbuf * 128u + (uint32_t)kk * 8u,
-                                   smem_desc_sw128(sV + (uint32_t)kk * 2048u, kHalfTile, 1024), kIdescPV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(bar(sb, PV_DONE + sbuf));
-                        mma_commit_mc(bar(sb, V_EMPTY + st), kClusterMask);
-                    }
+                    ++uq;
                 }
-                ++uq;
+                if (more) nxt = finish_unit(p, ahead, pairs, crank);
             }
             // Drain: every MMA issued above completes before TMEM is released.
             mma_commit(bar(sb, DRAIN));
@@ -1026,28 +1115,35 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         float* ls_s = reinterpret_cast<float*>(smem + pk::kSmLsum);
         bool failed = false;
         int gt = 0, uq = 0;
-        // The epilogue of a unit. Every softmax thread reaches it after the unit's
-        // tiles, failed or not, so that all of them meet at its barriers.
+        // The epilogue of a unit. Both warps of a row pair reach it after the
+        // unit's tiles, failed or not, so that they meet at its pair barrier.
         struct Pending {
             int b, kvh, n0, buf, last_gt;
             float m_used, l_part;
         };
         auto epilogue = [&](const Pending& e) {
-            // Only these eight warps write epi_skip, and only before the first
-            // barrier below, so after it every warp of the group takes the same branch.
-            bool ok = !failed;
-            if (ok)
-                ok = __all_sync(0xffffffffu, wait(bar(sb, PV_DONE + e.last_gt % kSBufs),
-                                                  (uint32_t)(e.last_gt / kSBufs) & 1u));
-            if (!ok) {
-                failed = true;
-                *epi_skip = 1;
-            }
+            // The row's two partial sums. The partner has read this slot's previous
+            // value: at least one pair barrier lies between.
             ls_s[half * 128 + row] = e.l_part;
-            named_barrier_sync(1, kSoftmaxThreads);
-            if (*epi_skip) return;
-            tc_fence_after();
+            if (!named_barrier_and(pair_bar, 64, !failed)) {
+                failed = true;
+                return;
+            }
             const float l_sum = ls_s[row] + ls_s[128 + row];
+            const int n = e.n0 + row / p.G;
+            if (half == 0 && p.lse != nullptr && n < p.N) {
+                const int h = e.kvh * p.G + row % p.G;
+                p.lse[((int64_t)e.b * p.Hq + h) * p.N + n] = (e.m_used + log2f(l_sum)) * 0.69314718055994531f;
+            }
+            // A warp whose wait fails skips the arrivals below; the roles waiting on
+            // them then see the abort flag, and its partner learns of the failure at
+            // the next pair barrier.
+            if (!__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + e.last_gt % kSBufs),
+                                              (uint32_t)(e.last_gt / kSBufs) & 1u))) {
+                failed = true;
+                return;
+            }
+            tc_fence_after();
             const float inv_l = 1.0f / l_sum;
             uint32_t r[2][32];
 #pragma unroll
@@ -1071,126 +1167,120 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     *reinterpret_cast<uint4*>(stage + off) = v;
                 }
             }
+            // The TMA store that the producer lane issues reads these bytes.
             fence_proxy_async_smem();
-            named_barrier_sync(1, kSoftmaxThreads);
-            if (threadIdx.x == 4 * 32) {
-                if (e.n0 < p.N) {
-                    const uint32_t sQ = sb + kSmQ0 + (uint32_t)e.buf * kTile;
-                    tma_store_4d(&tm_o, sQ, 0, e.kvh * p.G, e.n0, e.b);
-                    tma_store_4d(&tm_o, sQ + kHalfTile, 64, e.kvh * p.G, e.n0, e.b);
-                    tma_store_commit_and_wait_read();
-                }
-                mbar_arrive(bar(sb, Q_EMPTY + e.buf));   // the buffer may take a later unit's Q
-            }
-            const int n = e.n0 + row / p.G;
-            if (half == 0 && p.lse != nullptr && n < p.N) {
-                const int h = e.kvh * p.G + row % p.G;
-                p.lse[((int64_t)e.b * p.Hq + h) * p.N + n] = (e.m_used + log2f(l_sum)) * 0.69314718055994531f;
-            }
+            mbar_arrive(bar(sb, STAGED + e.buf));
         };
+        Unit nxt = cid < n_units ? decode(p, cid, pairs, crank) : Unit{};
         for (int U = cid; U < n_units; U += ncl) {
-            const Unit u = decode(p, U, pairs, crank);
-            if (u.n_tiles == 0) continue;
-            const int buf = uq & 1;
+            const Unit u = nxt;
+            const bool more = U + ncl < n_units;
+            const UnitLoad ahead = more ? load_unit(p, U + ncl, pairs) : UnitLoad{0, 0, 0};
             float m_used = -INFINITY;
             float l_part = 0.f;
-            // A failed wait sets `failed`: the loops then keep running without
-            // touching TMEM or the pipeline barriers, so that the two warps of a
-            // row pair still meet at every pair barrier.
-            for (int j = 0; j < u.n_tiles; ++j, ++gt) {
-                const int sbuf = gt % kSBufs;
-                const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
-                bool ok = !failed && __all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u));
-                float s[64];
-                float pmax = -INFINITY;
-                const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN)
-                                                   : min(kBlockN, p.N - (j - u.n_pre) * kBlockN);
-                const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
-                const bool masked = valid < 64;              // the same for the whole warp
-                float* mx_tile = mx_s + (gt & 1) * 256;
-                if (ok) {
-                    tc_fence_after();
-                    {
-                        uint32_t r[64];
-                        tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
-                    }
-                    // Keys past the end of the prefix or image segment do not exist.
-                    if (masked) {
-                        // An opaque statement keeps this block behind its branch: the
-                        // compiler would otherwise turn it into selects run on every tile.
-                        asm volatile("");
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
-                    }
-                    // Partial row maximum of the raw logits (three-input max tree).
-                    float t1[22];
-#pragma unroll
-                    for (int i = 0; i < 21; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-                    t1[21] = s[63];
-                    float t2[8];
-#pragma unroll
-                    for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
-                    t2[7] = t1[21];
-                    pmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
-                    mx_tile[half * 128 + row] = pmax;
-                }
-                // The other half's maximum comes through shared memory; both warps of
-                // the pair leave this barrier with the same verdict, and both have read
-                // all of S into registers, so either may then overwrite it with P.
-                tc_fence_before();
-                ok = named_barrier_and(pair_bar, 64, ok);
-                failed = !ok;
-                if (failed) continue;
-                tc_fence_after();
-                const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
-                const float m_new = fmaxf(m_used, mraw * p.scale_log2);
-                const bool need = m_new > m_used + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-                    if (need) m_used = m_new;
-                    l_part *= alpha;
-                    if (j > 0) {
-                        failed = !__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + (gt - 1) % kSBufs),
-                                                               (uint32_t)((gt - 1) / kSBufs) & 1u));
-                        if (failed) continue;
+            if (u.n_tiles > 0) {
+                // A failed wait sets `failed`: the loops then keep running without
+                // touching TMEM or the pipeline barriers, so that the two warps of a
+                // row pair still meet at every pair barrier.
+                for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                    const int sbuf = gt % kSBufs;
+                    const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
+                    bool ok = !failed && __all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u));
+                    float s[64];
+                    float pmax = -INFINITY;
+                    const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN)
+                                                       : min(kBlockN, p.N - (j - u.n_pre) * kBlockN);
+                    const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
+                    const bool masked = valid < 64;              // the same for the whole warp
+                    float* mx_tile = mx_s + (gt & 1) * 256;
+                    if (ok) {
                         tc_fence_after();
-                        uint32_t r[32];
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const uint32_t ocol = lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u;
-                            tmem_ld32(ocol, r);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_st32(ocol, r);
+                        {
+                            uint32_t r[64];
+                            tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
+    #pragma unroll
+                            for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
                         }
-                        tmem_st_wait();
+                        // Keys past the end of the prefix or image segment do not exist.
+                        if (masked) {
+                            // An opaque statement keeps this block behind its branch: the
+                            // compiler would otherwise turn it into selects run on every tile.
+                            asm volatile("");
+    #pragma unroll
+                            for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                        }
+                        // Partial row maximum of the raw logits (three-input max tree).
+                        float t1[22];
+    #pragma unroll
+                        for (int i = 0; i < 21; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+                        t1[21] = s[63];
+                        float t2[8];
+    #pragma unroll
+                        for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+                        t2[7] = t1[21];
+                        pmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
+                        mx_tile[half * 128 + row] = pmax;
                     }
+                    // The other half's maximum comes through shared memory; both warps of
+                    // the pair leave this barrier with the same verdict, and both have read
+                    // all of S into registers, so either may then overwrite it with P.
+                    tc_fence_before();
+                    ok = named_barrier_and(pair_bar, 64, ok);
+                    failed = !ok;
+                    if (failed) continue;
+                    tc_fence_after();
+                    const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
+                    const float m_new = fmaxf(m_used, mraw * p.scale_log2);
+                    const bool need = m_new > m_used + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                        if (need) m_used = m_new;
+                        l_part *= alpha;
+                        if (j > 0) {
+                            failed = !__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + (gt - 1) % kSBufs),
+                                                                   (uint32_t)((gt - 1) / kSBufs) & 1u));
+                            if (failed) continue;
+                            tc_fence_after();
+                            uint32_t r[32];
+    #pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                const uint32_t ocol = lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u;
+                                tmem_ld32(ocol, r);
+    #pragma unroll
+                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                                tmem_st32(ocol, r);
+                            }
+                            tmem_st_wait();
+                        }
+                    }
+                    // p = 2^(s*scale*log2e - m): a hidden key's -inf logit stays -inf
+                    // (the scale is > 0 and m finite from the first tile on), so its p is 0.
+                    const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nm = make_float2(-m_used, -m_used);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+                    uint32_t pk[32];
+    #pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
+                        const float2 e = make_float2(ex2(a.x), ex2(a.y));
+                        acc[c & 3] = fadd2(acc[c & 3], e);
+                        pk[c] = pack_bf16x2(e.x, e.y);
+                    }
+                    l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                              ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+                    tmem_st32(lane_base + scol + (uint32_t)half * 32u, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar(sb, P_FULL + sbuf));
                 }
-                // p = 2^(s*scale*log2e - m): a hidden key's -inf logit stays -inf
-                // (the scale is > 0 and m finite from the first tile on), so its p is 0.
-                const float2 cc = make_float2(p.scale_log2, p.scale_log2);
-                const float2 nm = make_float2(-m_used, -m_used);
-                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                 make_float2(0.f, 0.f)};
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
-                    const float2 e = make_float2(ex2(a.x), ex2(a.y));
-                    acc[c & 3] = fadd2(acc[c & 3], e);
-                    pk[c] = pack_bf16x2(e.x, e.y);
-                }
-                l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                          ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-                tmem_st32(lane_base + scol + (uint32_t)half * 32u, pk);
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(bar(sb, P_FULL + sbuf));
             }
-            epilogue(Pending{u.b, u.kvh, u.n0, buf, gt - 1, m_used, l_part});
-            ++uq;
+            // Before the epilogue, whose wait for the last PV hides it.
+            if (more) nxt = finish_unit(p, ahead, pairs, crank);
+            if (u.n_tiles > 0) {
+                epilogue(Pending{u.b, u.kvh, u.n0, uq & 1, gt - 1, m_used, l_part});
+                ++uq;
+            }
         }
     }
 

@@ -942,7 +942,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 const int buf = st_next & 1;
                 const uint32_t sbar = bar(sb, STAGED + buf);
                 const uint32_t par = (uint32_t)(st_next >> 1) & 1u;
-                if (block ? !wait(sbar, par) : !mbar_try_wait(sbar, par)) return false;
+                if (block ? !wait(sbar, par) : !mbar_test_wait(sbar, par)) return false;
                 const int3 c = buf ? qc1 : qc0;
                 if (c.y < p.N) {
                     const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;

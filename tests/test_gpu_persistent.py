@@ -1,0 +1,77 @@
+"""The persistent full-mask attention kernel on shapes the workload suite does
+not reach: one unit with a very long prefix, a batch of more than a thousand
+short sequences with ragged and empty prefixes, and repeated launches (every
+launch must give the same bits)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from attention_neo_qknorm_gb300 import neo, synth
+from helpers import GpuLayer, SCALE, assert_bf16_close, f64, oracle_layer, take_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def check_device_ok():
+    st, word = neo.neo_get_device_error()
+    assert word == 0, f"device error word {word:#x}"
+
+
+def test_one_unit_with_a_long_prefix(gpu_lib):
+    """A 20000-token prefix: one unit of 158 key tiles per KV head."""
+    w = synth.small_workload(prefix=(20000,), grid=(8, 8), Hq=4, Hkv=1, B=1)
+    inp = synth.make_inputs(w, seed=5)
+    layer = GpuLayer(w, inp)
+    layer.norm_rope()
+    layer.attention()
+    torch.cuda.synchronize()
+    check_device_ok()
+    ref, ref_lse = oracle_layer(w, inp)
+    assert_bf16_close(f64(layer.out), ref, "long prefix vs oracle")
+    np.testing.assert_allclose(f64(layer.lse), ref_lse, rtol=1e-3, atol=2e-2)
+
+
+def test_repeated_launches_identical(gpu_lib):
+    """Ten launches in a row give the same bits."""
+    w = synth.small_workload(prefix=(1000, 300), grid=(24, 16), Hq=32, Hkv=8, B=2)
+    inp = synth.make_inputs(w, seed=3)
+    layer = GpuLayer(w, inp)
+    layer.norm_rope()
+    layer.attention()
+    torch.cuda.synchronize()
+    first, first_lse = layer.out.clone(), layer.lse.clone()
+    for _ in range(9):
+        layer.attention()
+    torch.cuda.synchronize()
+    check_device_ok()
+    assert torch.equal(layer.out, first)
+    assert torch.equal(layer.lse, first_lse)
+
+
+def test_many_short_sequences(gpu_lib):
+    """1100 sequences of 4 image tokens with prefixes of 0..39 tokens."""
+    g = torch.Generator().manual_seed(17)
+    B, N, Hq, Hkv, D = 1100, 4, 4, 1, 128
+    lens = torch.randint(0, 40, (B,), generator=g)
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0)
+    total = int(cu[-1])
+    q = torch.randn(B, N, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, N, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, N, Hkv, D, generator=g).to(torch.bfloat16)
+    kp = torch.randn(total, Hkv, D, generator=g).to(torch.bfloat16)
+    vp = torch.randn(total, Hkv, D, generator=g).to(torch.bfloat16)
+    dq, dk, dv, dkp, dvp, dcu = (t.cuda() for t in (q, k, v, kp, vp, cu))
+    out = torch.empty(B, N, Hq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device="cuda")
+    neo.neo_gen_attention(dq, dkp, dvp, dk, dv, dcu, int(lens.max()), out, scale=SCALE, lse=lse)
+    torch.cuda.synchronize()
+    check_device_ok()
+    seqs = [0, 1, 511, 1022, 1023, 1024, 1025, 1099] + [int(b) for b in np.flatnonzero(lens.numpy() == 0)[:4]]
+    rows = np.array([(b, n, h) for b in seqs for n in range(N) for h in range(Hq)])
+    ref, ref_lse = O.gen_attention(f64(q), f64(kp), f64(vp), f64(k), f64(v), cu.numpy(), SCALE, rows=rows)
+    assert_bf16_close(take_rows(f64(out.cpu()), rows), ref, "1100 sequences")
+    got_lse = np.array([f64(lse.cpu())[b, h, n] for b, n, h in rows])
+    np.testing.assert_allclose(got_lse, ref_lse, rtol=1e-3, atol=2e-2)

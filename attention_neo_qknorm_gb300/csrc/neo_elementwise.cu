@@ -423,31 +423,46 @@ scale_noise_kernel(float* z, const float* eps, int64_t n, float sigma) {
 // ---------------------------------------------------------------------------
 // Interleaved 2-D RoPE of the vision tower ([U15] §Vision tower): channels
 // [0, C/2) turn with the patch column, [C/2, C) with the patch row, pairs
-// (2i, 2i+1) share the angle pos * theta^(-2i/(C/2)). A thread owns four
-// consecutive channels (two pairs) of a patch; consecutive threads cover
-// consecutive channels, so every access is coalesced.
+// (2i, 2i+1) share the angle pos * theta^(-2i/(C/2)).
+//
+// A thread owns one 16-byte chunk of channels (8 bf16 or 4 fp32: 4 or 2
+// pairs) of a sequence of patches: the `lanes` threads of a token cover its
+// chunks with consecutive addresses, a block holds `tpb` tokens, and the
+// patches of one thread lie `stride` tokens apart. The chunk's frequencies
+// are computed once; a patch's (row, column) advances by (stride / cols,
+// stride % cols) with carries, so the loop divides nothing. kRopeU patches
+// are in flight per thread.
 // ---------------------------------------------------------------------------
 template <typename T>
-struct Quad;   // four consecutive channels
+struct Chunk16;   // 16 bytes of channels as floats
 
 template <>
-struct Quad<__nv_bfloat16> {
-    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[4]) {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+struct Chunk16<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[8]) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
+        }
     }
-    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&y)[4]) {
-        const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(y[2], y[3]);
-        *reinterpret_cast<uint2*>(p) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&y)[8]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
 
 template <>
-struct Quad<float> {
+struct Chunk16<float> {
+    static constexpr int kVec = 4;
     static __device__ __forceinline__ void load(const float* p, float (&x)[4]) {
         const float4 u = *reinterpret_cast<const float4*>(p);
         x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
@@ -457,47 +472,68 @@ struct Quad<float> {
     }
 };
 
+constexpr int kRopeThreads = 256;
+constexpr int kRopeU = 2;
+
 template <typename T>
-__global__ void __launch_bounds__(256)
-rope2d_interleaved_kernel(T* __restrict__ x, int64_t n_tokens, int rows, int cols, int C, float log2_theta) {
-    // Thread (tx, block b): channel quads tx, tx + blockDim.x, ... of patches
-    // b, b + gridDim.x, ...; the quad's two frequencies are computed once.
-    const int quads = C / 4;
+__global__ void __launch_bounds__(kRopeThreads)
+rope2d_interleaved_kernel(T* __restrict__ x, int64_t n_tokens, int rows, int cols, int C, int lanes, int tpb,
+                          float log2_theta) {
+    constexpr int kVec = Chunk16<T>::kVec;
+    constexpr int kPairs = kVec / 2;
+    const int chunks = C / kVec;
     const int d = C / 2;
     const int per_img = rows * cols;
-    for (int q = threadIdx.x; q < quads; q += blockDim.x) {
-        const int ch = q * 4;
-        const bool row_half = ch >= d;
-        const int i0 = (ch - (row_half ? d : 0)) >> 1;
-        float fh[2], fl[2];
+    const int lane = (int)threadIdx.x % lanes;
+    const int slot = (int)threadIdx.x / lanes;
+    if (slot >= tpb) return;
+    const int64_t stride = (int64_t)gridDim.x * tpb;            // tokens between a thread's patches
+    const int smod = (int)(stride % per_img);
+    const int dr = smod / cols, dc = smod % cols;
+    const int64_t tok0 = (int64_t)blockIdx.x * tpb + slot;
+    if (tok0 >= n_tokens) return;
+    const int t0 = (int)(tok0 % per_img);
+    for (int cc = lane; cc < chunks; cc += lanes) {
+        const int ch = cc * kVec;
+        float fh[kPairs];
+        bool by_row[kPairs];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            fh[k] = exp2f(-2.0f * (float)(i0 + k) / (float)d * log2_theta);
-            fl[k] = 0.f;    // positions are patch indices: pos * f needs no extra precision
+        for (int k = 0; k < kPairs; ++k) {
+            const int c0 = ch + 2 * k;                           // first channel of the pair
+            by_row[k] = c0 >= d;
+            const int i = (c0 - (by_row[k] ? d : 0)) >> 1;
+            fh[k] = exp2f(-2.0f * (float)i / (float)d * log2_theta);
         }
-        constexpr int U = 4;   // patches in flight per thread
-        for (int64_t tb = blockIdx.x; tb < n_tokens; tb += (int64_t)gridDim.x * U) {
-            float v[U][4];
+        int r = t0 / cols, c = t0 % cols;
+        for (int64_t tok = tok0; tok < n_tokens; tok += (int64_t)kRopeU * stride) {
+            float v[kRopeU][kVec];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t tok = tb + (int64_t)u * gridDim.x;
-                if (tok < n_tokens) Quad<T>::load(x + tok * C + ch, v[u]);
+            for (int u = 0; u < kRopeU; ++u) {
+                const int64_t t = tok + (int64_t)u * stride;
+                if (t < n_tokens) Chunk16<T>::load(x + t * C + ch, v[u]);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t tok = tb + (int64_t)u * gridDim.x;
-                if (tok >= n_tokens) continue;
-                const int t = (int)(tok % per_img);
-                const float pos = (float)(row_half ? t / cols : t % cols);
-                float o[4];
+            for (int u = 0; u < kRopeU; ++u) {
+                const int64_t t = tok + (int64_t)u * stride;
+                if (t < n_tokens) {
+                    float o[kVec];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    float sn, cs;
-                    rope_sincos(pos, fh[k], fl[k], &sn, &cs);
-                    o[2 * k] = fmaf(v[u][2 * k], cs, -v[u][2 * k + 1] * sn);
-                    o[2 * k + 1] = fmaf(v[u][2 * k + 1], cs, v[u][2 * k] * sn);
+                    for (int k = 0; k < kPairs; ++k) {
+                        float sn, cs;
+                        rope_sincos((float)(by_row[k] ? r : c), fh[k], 0.f, &sn, &cs);
+                        o[2 * k] = fmaf(v[u][2 * k], cs, -v[u][2 * k + 1] * sn);
+                        o[2 * k + 1] = fmaf(v[u][2 * k + 1], cs, v[u][2 * k] * sn);
+                    }
+                    Chunk16<T>::store(x + t * C + ch, o);
                 }
-                Quad<T>::store(x + tok * C + ch, o);
+                // The next patch of this thread: (r, c) + (dr, dc) within its image.
+                c += dc;
+                if (c >= cols) {
+                    c -= cols;
+                    ++r;
+                }
+                r += dr;
+                if (r >= rows) r -= rows;
             }
         }
     }
@@ -760,14 +796,20 @@ extern "C" neo_status neo_rope2d_interleaved(void* x, neo_dtype dtype, int64_t n
     if (!x || !neo::aligned16(x) || (dtype == NEO_BF16 && C % 8 != 0)) return NEO_ERR_INVALID_ARG;
     const float log2_theta = (float)std::log2((double)theta);
     if ((int64_t)rows * cols > 0x7fffffffLL) return NEO_ERR_UNSUPPORTED;
-    const int threads = std::min(256, C / 4);
-    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(n_tokens, (int64_t)sm_count() * 16));
+    // Threads of a token: one per 16-byte chunk, at most a block's worth.
+    const int chunks = C / (dtype == NEO_BF16 ? 8 : 4);
+    const int lanes = std::min(chunks, kRopeThreads);
+    const int tpb = kRopeThreads / lanes;                      // tokens a block holds
+    // One resident wave of 4 blocks an SM (measured best at the 128 x 128 x 1024
+    // patch grid against 2-16 blocks an SM and 1-8 patches in flight).
+    const int64_t want = (n_tokens + (int64_t)tpb * kRopeU - 1) / ((int64_t)tpb * kRopeU);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 4));
     if (dtype == NEO_BF16)
-        rope2d_interleaved_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
-            static_cast<__nv_bfloat16*>(x), n_tokens, rows, cols, C, log2_theta);
+        rope2d_interleaved_kernel<__nv_bfloat16><<<(unsigned)blocks, lanes * tpb, 0, stream>>>(
+            static_cast<__nv_bfloat16*>(x), n_tokens, rows, cols, C, lanes, tpb, log2_theta);
     else
-        rope2d_interleaved_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(static_cast<float*>(x), n_tokens,
-                                                                                    rows, cols, C, log2_theta);
+        rope2d_interleaved_kernel<float><<<(unsigned)blocks, lanes * tpb, 0, stream>>>(
+            static_cast<float*>(x), n_tokens, rows, cols, C, lanes, tpb, log2_theta);
     return neo::launch_status();
 }
 

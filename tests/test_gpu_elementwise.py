@@ -194,6 +194,10 @@ def test_scale_noise_and_sampler_loop(gpu_lib):
     (torch.bfloat16, 2, 5, 7, 1024),      # model width, ragged grid
     (torch.bfloat16, 1, 128, 128, 1024),  # the 2048^2 patch grid (before the 2x2 merge)
     (torch.float32, 3, 4, 6, 64),
+    (torch.bfloat16, 3, 9, 5, 24),        # 8-channel chunks straddle the column/row halves
+    (torch.bfloat16, 1, 3, 4, 4096),      # more 16-byte chunks per patch than threads per block
+    (torch.bfloat16, 700, 3, 3, 8),       # one chunk per patch: many patches per block
+    (torch.float32, 2, 7, 3, 12),         # fp32 chunks straddle the halves
 ])
 def test_rope2d_interleaved_matches_oracle(gpu_lib, dtype, n_img, rows, cols, C):
     gen = torch.Generator().manual_seed(rows * cols + C)

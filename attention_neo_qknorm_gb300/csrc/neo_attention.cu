@@ -765,6 +765,16 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 //   * K and V rings, S buffers and the pair exchange run on one tile counter
 //     across units. K has two stages here to make room for the second Q.
 // The softmax of a tile is the same as in gen_attention_kernel.
+//
+// Block-causal instantiation (kBC, one sequence: a prefill): the temporal-
+// index range of every 64-key half of the image tiles is computed once per
+// CTA into shared memory. A unit's key tiles are the prefix tiles, the image
+// tiles up to the one holding its last query (the diagonal), and the later
+// image tiles with a half whose range meets the unit's queries' range (a
+// superset of the tiles holding a key with T_j == T_i); every role walks that
+// sequence with the same cursor. Units are taken pair-major (unit U: KV head
+// U % Hkv, query-tile pair U / Hkv), so that each cluster's share mixes
+// early, cheap query tiles with late, expensive ones.
 namespace pk {
 
 constexpr int kKStages = 2;
@@ -776,7 +786,10 @@ constexpr uint32_t kSmK = 2 * kTile;
 constexpr uint32_t kSmV = kSmK + kKStages * kTile;
 constexpr uint32_t kSmMax = kSmV + kVStages * kTile;   // float [2 tile parity][2 halves][128 rows]
 constexpr uint32_t kSmLsum = kSmMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]
-constexpr uint32_t kSmBar = kSmLsum + 2 * 128 * 4;
+constexpr uint32_t kSmTileTP = kSmLsum + 2 * 128 * 4;  // int4 [kMaxImgTiles] (kBC): min0 max0 min1 max1
+constexpr int kMaxUnitsBC = 2048;                      // kBC: units a cluster may take (host-checked)
+constexpr uint32_t kSmUnitTiles = kSmTileTP + kMaxImgTiles * 16;   // int [kMaxUnitsBC] (kBC): key tiles of unit k
+constexpr uint32_t kSmBar = kSmUnitTiles + kMaxUnitsBC * 4;
 
 enum : int {
     Q_FULL = 0,                                    // [2]
@@ -805,7 +818,18 @@ __device__ __forceinline__ uint32_t bar(uint32_t sbase, int i) { return sbase + 
 struct Unit {
     int b, kvh, n0, lo, L, n_pre, n_tiles;
     bool ok;                                       // consistent prefix offsets
+    int j_diag, tmin, tmax;                        // kBC: the diagonal image tile; the queries' T range
 };
+
+// kBC: the image tile after t (-1: the first) in a unit's key sequence.
+__device__ __forceinline__ int bc_next(const int4* tile_t, const Unit& u, int t, int n_img) {
+    if (t < u.j_diag) return t + 1;
+    for (int x = t + 1; x < n_img; ++x) {
+        const int4 r = tile_t[x];
+        if ((r.x <= u.tmax && r.y >= u.tmin) || (r.z <= u.tmax && r.w >= u.tmin)) return x;
+    }
+    return n_img;
+}
 
 // The prefix offsets of unit U's sequence. Every role loads them a unit
 // ahead: the loads are issued when a unit starts and their values are first
@@ -826,29 +850,80 @@ __device__ __forceinline__ UnitLoad load_unit(const AttnParams& p, int U, int pa
     return UnitLoad{U, ld_nc_s32(p.cu_prefix + b), ld_nc_s32(p.cu_prefix + b + 1)};
 }
 
-__device__ __forceinline__ Unit finish_unit(const AttnParams& p, const UnitLoad& l, int pairs, uint32_t crank) {
+// kBC: kWarp = all 32 lanes of the calling warp take part (the tile count is
+// then a ballot over the tiles past the diagonal instead of a serial walk).
+template <bool kBC, bool kWarp = false>
+__device__ __forceinline__ Unit finish_unit(const AttnParams& p, const UnitLoad& l, int pairs, uint32_t crank,
+                                            const uint8_t* smem) {
     Unit u;
-    const int per_b = p.Hkv * pairs;
-    u.b = l.U / per_b;
-    const int r = l.U - u.b * per_b;
-    u.kvh = r / pairs;
-    const int pair = r - u.kvh * pairs;
+    int pair;
+    if constexpr (kBC) {
+        u.b = 0;
+        u.kvh = l.U % p.Hkv;
+        pair = l.U / p.Hkv;
+    } else {
+        const int per_b = p.Hkv * pairs;
+        u.b = l.U / per_b;
+        const int r = l.U - u.b * per_b;
+        u.kvh = r / pairs;
+        pair = r - u.kvh * pairs;
+    }
     u.n0 = (pair * kCluster + (int)crank) * p.tok_per_tile;
     u.lo = l.lo;
     const int hi = l.hi;
     u.L = hi - u.lo;
     u.ok = !(u.lo < 0 || u.L < 0 || (int64_t)hi > p.total_prefix || u.L > p.max_prefix);
     u.n_pre = (u.L + kBlockN - 1) / kBlockN;
-    u.n_tiles = u.ok ? u.n_pre + (p.N + kBlockN - 1) / kBlockN : 0;
+    const int n_img = (p.N + kBlockN - 1) / kBlockN;
+    u.n_tiles = u.ok ? u.n_pre + n_img : 0;
+    u.j_diag = n_img - 1;
+    u.tmin = INT_MIN;
+    u.tmax = INT_MAX;
+    if constexpr (kBC) {
+        // The cluster's queries are image tokens [np0, np1): their T range from
+        // the 64-key halves holding them (a superset for pairs of under 64 tokens).
+        const int4* tile_t = reinterpret_cast<const int4*>(smem + kSmTileTP);
+        const int np0 = pair * kCluster * p.tok_per_tile;
+        const int np1 = min(p.N, np0 + kCluster * p.tok_per_tile);
+        u.j_diag = (np1 - 1) / kBlockN;
+        u.tmin = INT_MAX;
+        u.tmax = INT_MIN;
+        for (int h = np0 / 64; h <= (np1 - 1) / 64; ++h) {
+            const int4 r = tile_t[h >> 1];
+            u.tmin = min(u.tmin, (h & 1) ? r.z : r.x);
+            u.tmax = max(u.tmax, (h & 1) ? r.w : r.y);
+        }
+        if constexpr (kWarp) {
+            // All 32 lanes: count the image tiles of the unit's key sequence.
+            const int lane = (int)(threadIdx.x & 31);
+            int cnt = u.j_diag + 1;
+            for (int t0 = u.j_diag + 1; t0 < n_img; t0 += 32) {
+                bool kept = false;
+                if (t0 + lane < n_img) {
+                    const int4 r = tile_t[t0 + lane];
+                    kept = (r.x <= u.tmax && r.y >= u.tmin) || (r.z <= u.tmax && r.w >= u.tmin);
+                }
+                cnt += __popc(__ballot_sync(0xffffffffu, kept));
+            }
+            u.n_tiles = u.ok ? u.n_pre + cnt : 0;
+        } else {
+            // Counted once in the prologue (unit k of this cluster: U = cluster + k * clusters).
+            const int ncl = (int)(gridDim.x / kCluster), cid = (int)(blockIdx.x / kCluster);
+            const int cnt = reinterpret_cast<const int*>(smem + kSmUnitTiles)[(l.U - cid) / ncl];
+            u.n_tiles = u.ok ? u.n_pre + cnt : 0;
+        }
+    }
     return u;
 }
 
-__device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, uint32_t crank) {
-    return finish_unit(p, load_unit(p, U, pairs), pairs, crank);
+template <bool kBC, bool kWarp = false>
+__device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, uint32_t crank, const uint8_t* smem) {
+    return finish_unit<kBC, kWarp>(p, load_unit(p, U, pairs), pairs, crank, smem);
 }
 
 }  // namespace pk
 
+template <bool kBC>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                                 const __grid_constant__ CUtensorMap tm_kimg,
@@ -903,6 +978,46 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         tmem_alloc(sb + pk::kSmTmemSlot, kTmCols);
         tmem_relinquish();
     }
+    const int n_img = (p.N + kBlockN - 1) / kBlockN;
+    if constexpr (kBC) {
+        // One warp per image tile: the temporal-index range of each 64-key half
+        // (empty halves past the last key: [INT_MAX, INT_MIN]).
+        // Four tiles a warp at a time, all loads issued before any is used.
+        int4* tile_t = reinterpret_cast<int4*>(smem + pk::kSmTileTP);
+        constexpr int kW = kThreads / 32;
+        for (int t0 = warp; t0 < n_img; t0 += 4 * kW) {
+            int tk[4][kBlockN / 32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int c = 0; c < kBlockN / 32; ++c) {
+                    const int key = (t0 + q * kW) * kBlockN + c * 32 + lane;
+                    tk[q][c] = key < p.N ? __ldg(p.t_img + key) : INT_MIN;
+                }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int t = t0 + q * kW;
+                if (t >= n_img) break;   // warp-uniform
+                int lo2[2] = {INT_MAX, INT_MAX}, hi2[2] = {INT_MIN, INT_MIN};
+#pragma unroll
+                for (int c = 0; c < kBlockN / 32; ++c)
+                    if (t * kBlockN + c * 32 + lane < p.N) {
+                        lo2[c >> 1] = min(lo2[c >> 1], tk[q][c]);
+                        hi2[c >> 1] = max(hi2[c >> 1], tk[q][c]);
+                    }
+                const int4 range = make_int4(__reduce_min_sync(0xffffffffu, lo2[0]), __reduce_max_sync(0xffffffffu, hi2[0]),
+                                             __reduce_min_sync(0xffffffffu, lo2[1]), __reduce_max_sync(0xffffffffu, hi2[1]));
+                if (lane == 0) tile_t[t] = range;
+            }
+        }
+        __syncthreads();
+        // The image key tiles of each of this cluster's units, one warp a unit.
+        int* unit_tiles = reinterpret_cast<int*>(smem + pk::kSmUnitTiles);
+        for (int k = warp; cid + k * ncl < n_units; k += kThreads / 32) {
+            const Unit u = pk::decode<true, true>(p, cid + k * ncl, pairs, 0, smem);
+            if (lane == 0) unit_tiles[k] = u.n_tiles - u.n_pre;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     // No CTA may multicast into a peer before the peer's barriers exist.
@@ -913,7 +1028,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     if (threadIdx.x == 0) {
         // Report inconsistent prefix offsets once per CTA; such units are skipped by every role.
         for (int U = cid; U < n_units; U += ncl)
-            if (!decode(p, U, pairs, crank).ok) {
+            if (!decode<kBC>(p, U, pairs, crank, smem).ok) {
                 atomicOr(&g_dev_error, NEO_DEVERR_BAD_PREFIX);
                 break;
             }
@@ -970,14 +1085,18 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 q_issued = uqi;
                 return true;
             };
-            Unit nxt = cid < n_units ? decode(p, cid, pairs, crank) : Unit{};
+            Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
             for (int U = cid; ok && U < n_units; U += ncl) {
                 const Unit u = nxt;
                 const bool more = U + ncl < n_units;
                 const UnitLoad ahead = more ? load_unit(p, U + ncl, pairs) : UnitLoad{0, 0, 0};
                 if (u.n_tiles > 0) {
                     if (is_k && uq == 0) ok = issue_q(u, 0);
+                    int it = -1;                   // image tile of key tile j
                     for (int j = 0; ok && j < u.n_tiles; ++j) {
+                        if (j >= u.n_pre)
+                            it = kBC ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
+                                     : j - u.n_pre;
                         const int st = gt % stages;
                         if (!wait(bar(sb, empty0 + st), ((uint32_t)(gt / stages) & 1u) ^ 1u)) {
                             ok = false;
@@ -991,7 +1110,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                         if (j < u.n_pre)
                             tma_load_3d_mc(hdst, pre_map, fb, d0, u.kvh, u.lo + j * kBlockN, kClusterMask);
                         else
-                            tma_load_4d_mc(hdst, img_map, fb, d0, u.kvh, (j - u.n_pre) * kBlockN, u.b, kClusterMask);
+                            tma_load_4d_mc(hdst, img_map, fb, d0, u.kvh, it * kBlockN, u.b, kClusterMask);
                         ++gt;
                         if (is_k && st_next < uq) store_next(false);
                         // The next unit's Q, kQLead tiles before this unit's last K tile.
@@ -999,15 +1118,15 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                         // epilogue needs none of this unit's loads.
                         if (is_k && more && j == max(0, u.n_tiles - kQLead)) {
                             // The next non-empty unit (empty ones come only from bad prefix offsets).
-                            Unit u2 = finish_unit(p, ahead, pairs, crank);
+                            Unit u2 = finish_unit<kBC>(p, ahead, pairs, crank, smem);
                             for (int U2 = U + 2 * ncl; u2.n_tiles == 0 && U2 < n_units; U2 += ncl)
-                                u2 = decode(p, U2, pairs, crank);
+                                u2 = decode<kBC>(p, U2, pairs, crank, smem);
                             if (u2.n_tiles > 0) ok = issue_q(u2, uq + 1);
                         }
                     }
                     ++uq;
                 }
-                if (more) nxt = finish_unit(p, ahead, pairs, crank);
+                if (more) nxt = finish_unit<kBC>(p, ahead, pairs, crank, smem);
             }
             if (is_k) {
                 // The outputs of the last units; then every store has read its tile.
@@ -1031,7 +1150,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         if (lane == 0) {
             bool ok = true;
             int gt = 0, uq = 0;
-            Unit nxt = cid < n_units ? decode(p, cid, pairs, crank) : Unit{};
+            Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
             for (int U = cid; ok && U < n_units; U += ncl) {
                 const Unit u = nxt;
                 const bool more = U + ncl < n_units;
@@ -1097,7 +1216,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     }
                     ++uq;
                 }
-                if (more) nxt = finish_unit(p, ahead, pairs, crank);
+                if (more) nxt = finish_unit<kBC>(p, ahead, pairs, crank, smem);
             }
             // Drain: every MMA issued above completes before TMEM is released.
             mma_commit(bar(sb, DRAIN));
@@ -1171,7 +1290,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             fence_proxy_async_smem();
             mbar_arrive(bar(sb, STAGED + e.buf));
         };
-        Unit nxt = cid < n_units ? decode(p, cid, pairs, crank) : Unit{};
+        Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
         for (int U = cid; U < n_units; U += ncl) {
             const Unit u = nxt;
             const bool more = U + ncl < n_units;
@@ -1179,19 +1298,57 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             float m_used = -INFINITY;
             float l_part = 0.f;
             if (u.n_tiles > 0) {
+                // kBC: this row's query is image token n_row (clamped for padding
+                // rows, whose output is never stored), i_row = L + n_row in the
+                // concatenated order [prefix ; image], with temporal index t_row.
+                const int n_row = min(u.n0 + row / p.G, p.N - 1);
+                const int i_row = u.L + n_row;
+                const int t_row = kBC ? __ldg(p.t_img + n_row) : 0;
+                int it = -1;                       // image tile of key tile j
                 // A failed wait sets `failed`: the loops then keep running without
                 // touching TMEM or the pipeline barriers, so that the two warps of a
                 // row pair still meet at every pair barrier.
                 for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                    if (j >= u.n_pre)
+                        it = kBC ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
+                                 : j - u.n_pre;
                     const int sbuf = gt % kSBufs;
                     const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
                     bool ok = !failed && __all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u));
                     float s[64];
                     float pmax = -INFINITY;
-                    const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN)
-                                                       : min(kBlockN, p.N - (j - u.n_pre) * kBlockN);
+                    const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
                     const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
-                    const bool masked = valid < 64;              // the same for the whole warp
+                    bool partial = valid < 64;
+                    uint64_t keep = 0;                           // kBC: bit c = key column c is visible
+                    if constexpr (kBC) {
+                        // Key j of [prefix ; image] is visible to query i iff T_j == T_i or
+                        // j <= i ("Block-causal attention"). This row's 64 keys: all at or
+                        // before the row or all sharing its index -> the segment-end mask
+                        // only; the row's index outside the keys' range -> causal, a
+                        // threshold; otherwise (a block boundary) key by key.
+                        const int key0 = (j < u.n_pre ? j * kBlockN : u.L + it * kBlockN) + half * 64;
+                        keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
+                        if (j >= u.n_pre && key0 + 63 > i_row) {
+                            const int4 tr = reinterpret_cast<const int4*>(smem + pk::kSmTileTP)[it];
+                            const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
+                            if (!(klo == t_row && khi == t_row)) {
+                                const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
+                                const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
+                                if (t_row < klo || t_row > khi) {
+                                    keep &= causal;
+                                } else {
+                                    const int32_t* tk = p.t_img + (key0 - u.L);
+                                    for (int c = max(lim, 0); c < min(valid, 64); ++c)
+                                        if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
+                                }
+                            }
+                        }
+                        partial = keep != ~0ull;
+                    }
+                    // Warp-uniform, so that the per-element mask below is a branch that
+                    // full tiles skip (with the full mask it depends on the tile only).
+                    const bool masked = kBC ? __any_sync(0xffffffffu, partial) : partial;
                     float* mx_tile = mx_s + (gt & 1) * 256;
                     if (ok) {
                         tc_fence_after();
@@ -1207,7 +1364,12 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                             // compiler would otherwise turn it into selects run on every tile.
                             asm volatile("");
     #pragma unroll
-                            for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                            for (int c = 0; c < 64; ++c) {
+                                bool vis;
+                                if constexpr (kBC) vis = (keep >> c) & 1u;
+                                else vis = c < valid;
+                                s[c] = vis ? s[c] : -INFINITY;
+                            }
                         }
                         // Partial row maximum of the raw logits (three-input max tree).
                         float t1[22];
@@ -1276,7 +1438,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 }
             }
             // Before the epilogue, whose wait for the last PV hides it.
-            if (more) nxt = finish_unit(p, ahead, pairs, crank);
+            if (more) nxt = finish_unit<kBC>(p, ahead, pairs, crank, smem);
             if (u.n_tiles > 0) {
                 epilogue(Pending{u.b, u.kvh, u.n0, uq & 1, gt - 1, m_used, l_part});
                 ++uq;
@@ -1437,9 +1599,11 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         for (const void* k : kernels)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(gen_attention_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)pk::kSmemBytes);
+        const void* persistent[2] = {(const void*)gen_attention_persistent_kernel<false>,
+                                     (const void*)gen_attention_persistent_kernel<true>};
+        for (const void* k : persistent)
+            if (attr_err == cudaSuccess)
+                attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
 
@@ -1471,9 +1635,10 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     // computes and stores nothing of its own but still shares the K/V stream).
     const int qtiles = (N + tok_per_tile - 1) / tok_per_tile;
     const bool bc = mask_mode == NEO_MASK_BLOCK_CAUSAL;
-    if (!bc && !qn) {
-        // Full mask: the persistent kernel, one cluster per pair of SMs it can
-        // keep resident, each working through its share of the units.
+    if (!qn && (!bc || B == 1)) {
+        // Full mask, and the block-causal mask of one sequence (a prefill): the
+        // persistent kernel, one cluster per pair of SMs it can keep resident,
+        // each working through its share of the units.
         static std::once_flag occ_once;
         static int max_clusters = 0;
         std::call_once(occ_once, [] {
@@ -1488,8 +1653,8 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
             cfg.dynamicSmemBytes = pk::kSmemBytes;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void*)gen_attention_persistent_kernel, &cfg) !=
-                cudaSuccess)
+            if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void*)gen_attention_persistent_kernel<false>,
+                                               &cfg) != cudaSuccess)
                 max_clusters = 0;
             cudaGetLastError();
         });
@@ -1498,10 +1663,19 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         const int64_t n_units = (int64_t)B * Hkv * pairs;
         if (n_units > 0x7fffffffLL) return NEO_ERR_UNSUPPORTED;
         const int clusters = (int)std::min<int64_t>(n_units, max_clusters);
-        gen_attention_persistent_kernel<<<dim3((unsigned)(clusters * kCluster)), kThreads, pk::kSmemBytes, stream>>>(
-            tq, to, tki, tvi, tkp, tvp, prm, (int)n_units, pairs);
-        return neo::launch_status();
+        // A one-sequence block-causal launch keeps one tile count per unit of a
+        // cluster in shared memory (at most pk::kMaxUnitsBC of them); beyond that
+        // it takes the one-tile-per-CTA kernel below.
+        if (!bc || (n_units + clusters - 1) / clusters <= pk::kMaxUnitsBC) {
+            // (both instantiations use the same threads and shared memory)
+            auto kernel = bc ? gen_attention_persistent_kernel<true> : gen_attention_persistent_kernel<false>;
+            kernel<<<dim3((unsigned)(clusters * kCluster)), kThreads, pk::kSmemBytes, stream>>>(
+                tq, to, tki, tvi, tkp, tvp, prm, (int)n_units, pairs);
+            return neo::launch_status();
+        }
     }
+    // The folded query norm, and the block-causal mask of several sequences:
+    // one query tile per CTA.
     const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
     auto kernel = bc ? (qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>)
                      : gen_attention_kernel<false, true>;

@@ -239,3 +239,55 @@ def test_many_short_units_per_cluster(gpu_lib):
     prefix = tuple(int(x) for x in rng.integers(0, 120, size=300))
     out = run_case(prefix, 40, 4, 1, seed=13)
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("case", ["mixed", "chunked", "unordered", "random", "g1"])
+def test_block_causal_one_sequence_equals_batched(gpu_lib, case):
+    """One sequence runs in the persistent kernel, a batch of two in the
+    one-tile-per-CTA kernel; each sequence of the batch, run alone, gives the
+    same bits (tiles the persistent kernel keeps beyond the exact set are fully
+    masked and add exact zeros)."""
+    rng = np.random.default_rng(21)
+    Hq, Hkv = 8, 2
+    if case == "mixed":
+        pre, img = [[], []], [_mixed_T(40, 64, 25), _mixed_T(7, 64, 58)]
+    elif case == "chunked":
+        a, b = _mixed_T(30, 100, 70), _mixed_T(60, 64, 76)
+        pre, img, Hq, Hkv = [a[:70], b[:70]], [a[70:], b[70:]], 4, 1
+    elif case == "unordered":
+        T = list(range(300)) + [5] * 100 + list(range(300, 500))
+        pre, img = [[], []], [T, T[::-1]]
+    elif case == "random":
+        pre = [rng.integers(0, 40, size=50).tolist(), rng.integers(0, 400, size=90).tolist()]
+        img = [rng.integers(0, 40, size=333).tolist(), rng.integers(0, 400, size=333).tolist()]
+    else:
+        pre, img, Hq, Hkv = [[], []], [_mixed_T(100, 256, 20), _mixed_T(20, 256, 100)], 2, 2
+    B, N = 2, len(img[0])
+    Ls = [len(t) for t in pre]
+    g = torch.Generator().manual_seed(33)
+    bf = lambda *sh: torch.randn(*sh, generator=g).to(torch.bfloat16).cuda()
+    q, k, v = bf(B, N, Hq, 128), bf(B, N, Hkv, 128), bf(B, N, Hkv, 128)
+    total = sum(Ls)
+    kp, vp = (bf(total, Hkv, 128), bf(total, Hkv, 128)) if total else (None, None)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(Ls)]), dtype=torch.int32, device="cuda")
+    t_pre = torch.tensor(np.concatenate([np.asarray(t, np.int32) for t in pre]) if total else np.zeros(0, np.int32),
+                         dtype=torch.int32, device="cuda")
+    t_img = torch.tensor(np.asarray(img, np.int32).reshape(-1), device="cuda")
+    out = torch.empty(B, N, Hq, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device="cuda")
+    neo.neo_gen_attention(q, kp, vp, k, v, cu, max(Ls), out, scale=SCALE, lse=lse,
+                          mask_mode=neo.NEO_MASK_BLOCK_CAUSAL, t_prefix=t_pre if total else None, t_img=t_img)
+    for b in range(B):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        o1 = torch.empty(1, N, Hq, 128, dtype=torch.bfloat16, device="cuda")
+        l1 = torch.empty(1, Hq, N, dtype=torch.float32, device="cuda")
+        cu1 = torch.tensor([0, hi - lo], dtype=torch.int32, device="cuda")
+        neo.neo_gen_attention(q[b:b + 1].contiguous(), kp[lo:hi].contiguous() if hi > lo else None,
+                              vp[lo:hi].contiguous() if hi > lo else None, k[b:b + 1].contiguous(),
+                              v[b:b + 1].contiguous(), cu1, hi - lo, o1, scale=SCALE, lse=l1,
+                              mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
+                              t_prefix=t_pre[lo:hi].contiguous() if hi > lo else None,
+                              t_img=t_img[b * N:(b + 1) * N].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], out[b]), f"{case}: sequence {b} differs between the two kernels"
+        assert torch.equal(l1[0], lse[b])

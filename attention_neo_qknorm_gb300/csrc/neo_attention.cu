@@ -240,6 +240,68 @@ __device__ __forceinline__ void qnorm_rope_q_half(uint8_t* half_tile, int row, c
     }
 }
 
+// As qnorm_rope_angles + qnorm_rope_q_half, with each chunk pair's eight
+// (cos, sin) computed where they are used instead of all 32 up front, and the
+// row's chunks read again from shared memory for the rotation instead of kept
+// in registers: the same calls and operations on the same values (hence the
+// same bits) in fewer registers.
+template <int half>
+__device__ __forceinline__ void qnorm_rope_q_half_lowreg(uint8_t* half_tile, int row, const float pos[3],
+                                                         const neo::RopeFreqs& fr, const float* w, float eps) {
+    uint8_t* rowp = half_tile + row * 128;
+    auto chunk = [&](int c) { return *reinterpret_cast<const uint4*>(rowp + ((c ^ (row & 7)) << 4)); };
+    auto unpack = [](uint4 u, float2 (&x)[4]) {
+        const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = make_float2(__uint_as_float(v[i] << 16), __uint_as_float(v[i] & 0xffff0000u));
+    };
+    constexpr int pa[4] = {0, 1, half ? 4 : 2, half ? 5 : 3};
+    constexpr int pb[4] = {half ? 2 : 4, half ? 3 : 5, 6, 7};
+    float part[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        float2 xa[4], xb[4];
+        unpack(chunk(pa[s]), xa);
+        unpack(chunk(pb[s]), xb);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = ffma2(xa[i], xa[i], ffma2(xb[i], xb[i], acc));
+        part[s] = acc.x + acc.y;
+    }
+    const float ss = (part[0] + part[1]) + (part[2] + part[3]);
+    const float rs = rsqrtf(ss * (1.0f / 64.0f) + eps);
+    const float2 rs2 = make_float2(rs, rs);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int pair0 = half ? (s < 2 ? 32 + 8 * s : 48 + 8 * (s - 2)) : 8 * s;
+        const float p_s = pos[half ? (s < 2 ? 1 : 2) : 0];
+        float cs[8], sn[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) neo::rope_sincos(p_s, fr.hi[pair0 + j], fr.lo[pair0 + j], &sn[j], &cs[j]);
+        float2 xa[4], xb[4];
+        unpack(chunk(pa[s]), xa);   // not yet written: chunk pairs are disjoint
+        unpack(chunk(pb[s]), xb);
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 wa = *reinterpret_cast<const float2*>(w + 8 * pa[s] + 2 * i);
+            const float2 wb = *reinterpret_cast<const float2*>(w + 8 * pb[s] + 2 * i);
+            const int e = 2 * i;
+            const float2 uc = make_float2(wa.x * cs[e], wa.y * cs[e + 1]);
+            const float2 vs = make_float2(-wb.x * sn[e], -wb.y * sn[e + 1]);
+            const float2 vc = make_float2(wb.x * cs[e], wb.y * cs[e + 1]);
+            const float2 us = make_float2(wa.x * sn[e], wa.y * sn[e + 1]);
+            const float2 u = fmul2(xa[i], rs2), v = fmul2(xb[i], rs2);
+            const float2 ya = ffma2(u, uc, fmul2(v, vs));
+            const float2 yb = ffma2(v, vc, fmul2(u, us));
+            oa[i] = pack_bf16x2(ya.x, ya.y);
+            ob[i] = pack_bf16x2(yb.x, yb.y);
+        }
+        *reinterpret_cast<uint4*>(rowp + ((pa[s] ^ (row & 7)) << 4)) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        *reinterpret_cast<uint4*>(rowp + ((pb[s] ^ (row & 7)) << 4)) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    }
+}
+
 // kQNorm: the query norm + RoPE is folded into the prologue (a separate
 // instantiation, so that the plain kernel's code is unchanged by it).
 template <bool kBlockCausal, bool kQNorm>
@@ -775,11 +837,28 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 // sequence with the same cursor. Units are taken pair-major (unit U: KV head
 // U % Hkv, query-tile pair U / Hkv), so that each cluster's share mixes
 // early, cheap query tiles with late, expensive ones.
+//
+// Folded query norm instantiation (kQN, the full mask): a fourth warpgroup
+// (warps 12-15) waits for each unit's raw Q tile, normalises its halves and
+// rotates it in shared memory (the arithmetic of the standalone norm/RoPE
+// kernel's bf16 path, hence the same bits) and arrives on Q_READY, which the
+// S issuer waits for instead of Q_FULL. The next unit's Q is loaded
+// kQLeadQN tiles ahead so that this work is hidden. setmaxnreg splits the
+// 512 x 128 registers of the launch: 72 a thread for the roles, 168 for the
+// softmax, 104 for the norm warpgroup (128 x 72 + 256 x 168 + 128 x 104 = 65536).
 namespace pk {
 
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kQLead = 4;                          // tiles ahead that the next Q is loaded
+constexpr int kQLeadQN = 12;                       // ... with the folded query norm
+constexpr int kThreadsQN = 512;                    // kQN: 16 warps
+constexpr int kQnWarp0 = 12;                       // kQN: the norm warpgroup, warps 12..15
+constexpr uint32_t kQnBar = 6;                     // its named barrier (2..5 are the row pairs')
+constexpr int kRegsLaunchQN = 65536 / kThreadsQN;      // registers a thread at launch (__launch_bounds__)
+constexpr int kRegsRolesQN = 72, kRegsSoftmaxQN = 168, kRegsNormQN = 104;
+static_assert(128 * kRegsRolesQN + 256 * kRegsSoftmaxQN + 128 * kRegsNormQN <= kThreadsQN * kRegsLaunchQN,
+              "register split above the launch's total");
 
 constexpr uint32_t kSmQ0 = 0;                      // Q buffers 0 and 1 (also output staging)
 constexpr uint32_t kSmK = 2 * kTile;
@@ -789,7 +868,8 @@ constexpr uint32_t kSmLsum = kSmMax + 2 * 2 * 128 * 4; // float [2 halves][128 r
 constexpr uint32_t kSmTileTP = kSmLsum + 2 * 128 * 4;  // int4 [kMaxImgTiles] (kBC): min0 max0 min1 max1
 constexpr int kMaxUnitsBC = 2048;                      // kBC: units a cluster may take (host-checked)
 constexpr uint32_t kSmUnitTiles = kSmTileTP + kMaxImgTiles * 16;   // int [kMaxUnitsBC] (kBC): key tiles of unit k
-constexpr uint32_t kSmBar = kSmUnitTiles + kMaxUnitsBC * 4;
+constexpr uint32_t kSmQnWP = kSmUnitTiles + kMaxUnitsBC * 4;   // float [128] (kQN): the q norm weights
+constexpr uint32_t kSmBar = kSmQnWP + 128 * 4;
 
 enum : int {
     Q_FULL = 0,                                    // [2]
@@ -803,7 +883,8 @@ enum : int {
     PV_DONE = P_FULL + kSBufs,
     O_FREE = PV_DONE + kSBufs,
     DRAIN = O_FREE + 1,
-    NUM_BARS = DRAIN + 1
+    Q_READY = DRAIN + 1,                           // [2] kQN: the unit's Q is normalised and rotated
+    NUM_BARS = Q_READY + 2
 };
 
 constexpr uint32_t kSmTmemSlot = kSmBar + NUM_BARS * 8;
@@ -923,14 +1004,14 @@ __device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, ui
 
 }  // namespace pk
 
-template <bool kBC>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kBC, bool kQN>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kQN ? pk::kThreadsQN : kThreads, 1)
 gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                                 const __grid_constant__ CUtensorMap tm_kimg,
                                 const __grid_constant__ CUtensorMap tm_vimg,
                                 const __grid_constant__ CUtensorMap tm_kpre,
                                 const __grid_constant__ CUtensorMap tm_vpre, const AttnParams p, int n_units,
-                                int pairs) {
+                                int pairs, const neo::RopeFreqs qn_freqs) {
     using pk::bar;
     using pk::decode;
     using pk::finish_unit;
@@ -967,6 +1048,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             uint32_t count = 1;
             if ((i >= P_FULL && i < P_FULL + kSBufs) || i == O_FREE || (i >= STAGED && i < STAGED + 2))
                 count = kSoftmaxThreads;
+            if (i >= pk::Q_READY && i < pk::Q_READY + 2) count = 128;   // the norm warpgroup
             if ((i >= K_EMPTY && i < K_EMPTY + pk::kKStages) || (i >= V_EMPTY && i < V_EMPTY + pk::kVStages))
                 count = kCluster;                // released by the MMA of every CTA of the cluster
             if (i == DRAIN) count = 2;          // one commit from each MMA issuer
@@ -1036,6 +1118,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers: Q, K and the output stores (warp 0), V (warp 2)
+        if constexpr (kQN) setmaxnreg_to<pk::kRegsRolesQN, pk::kRegsLaunchQN>();
         if (lane == 0) {
             const bool is_k = warp == 0;
             const int stages = is_k ? pk::kKStages : pk::kVStages;
@@ -1116,7 +1199,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                         // The next unit's Q, kQLead tiles before this unit's last K tile.
                         // Its buffer holds the output of the unit before this one, whose
                         // epilogue needs none of this unit's loads.
-                        if (is_k && more && j == max(0, u.n_tiles - kQLead)) {
+                        if (is_k && more && j == max(0, u.n_tiles - (kQN ? pk::kQLeadQN : kQLead))) {
                             // The next non-empty unit (empty ones come only from bad prefix offsets).
                             Unit u2 = finish_unit<kBC>(p, ahead, pairs, crank, smem);
                             for (int U2 = U + 2 * ncl; u2.n_tiles == 0 && U2 < n_units; U2 += ncl)
@@ -1147,6 +1230,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         __syncwarp();
     } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issuers
+        if constexpr (kQN) setmaxnreg_to<pk::kRegsRolesQN, pk::kRegsLaunchQN>();
         if (lane == 0) {
             bool ok = true;
             int gt = 0, uq = 0;
@@ -1159,7 +1243,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     if (warp == 1) {
                         const int buf = uq & 1;
                         const uint32_t sQ = sb + kSmQ0 + (uint32_t)buf * kTile;
-                        if (!wait(bar(sb, Q_FULL + buf), (uint32_t)(uq >> 1) & 1u)) break;
+                        if (!wait(bar(sb, (kQN ? pk::Q_READY : Q_FULL) + buf), (uint32_t)(uq >> 1) & 1u)) break;
                         tc_fence_after();
                         for (int j = 0; j < u.n_tiles; ++j, ++gt) {
                             const int st = gt % pk::kKStages;
@@ -1223,8 +1307,9 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             wait(bar(sb, DRAIN), 0, false);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp < 12) {
         // ------------------------------------------------------------ softmax + epilogue
+        if constexpr (kQN) setmaxnreg_to<pk::kRegsSoftmaxQN, pk::kRegsLaunchQN>();
         const int half = (warp - 4) >> 2;          // key columns [64*half, 64*half + 64)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
@@ -1444,6 +1529,41 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 ++uq;
             }
         }
+    } else if constexpr (kQN) {
+        // ------------------------------------------------------------ query norm + RoPE (warps 12..15)
+        // Thread t normalises and rotates both 64-dim halves of Q row t of each
+        // unit's tile in shared memory (128-byte swizzled, as the TMA wrote it).
+        setmaxnreg_to<pk::kRegsNormQN, pk::kRegsLaunchQN>();
+        const int t = (int)threadIdx.x - pk::kQnWarp0 * 32;
+        float* w_s = reinterpret_cast<float*>(smem + pk::kSmQnWP);
+        w_s[t] = t < 64 ? __ldg(p.qn_w_t + t) : __ldg(p.qn_w_hw + (t - 64));
+        named_barrier_sync(pk::kQnBar, 128);           // the weights are in shared memory
+        const int64_t S = (int64_t)p.B * p.N;
+        bool ok = true;
+        int uq = 0;
+        Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
+        for (int U = cid; ok && U < n_units; U += ncl) {
+            const Unit u = nxt;
+            const bool more = U + ncl < n_units;
+            const UnitLoad ahead = more ? load_unit(p, U + ncl, pairs) : UnitLoad{0, 0, 0};
+            if (u.n_tiles > 0) {
+                const int buf = uq & 1;
+                uint8_t* sQ = smem + kSmQ0 + (uint32_t)buf * kTile;
+                const int64_t tok = (int64_t)u.b * p.N + min(u.n0 + t / p.G, p.N - 1);
+                float pos[3];
+#pragma unroll
+                for (int a = 0; a < 3; ++a) pos[a] = (float)__ldg(p.qn_idx + a * S + tok);
+                ok = __all_sync(0xffffffffu, wait(bar(sb, Q_FULL + buf), (uint32_t)(uq >> 1) & 1u));
+                if (ok) {
+                    qnorm_rope_q_half_lowreg<0>(sQ, t, pos, qn_freqs, w_s, p.qn_eps);
+                    qnorm_rope_q_half_lowreg<1>(sQ + kHalfTile, t, pos, qn_freqs, w_s + 64, p.qn_eps);
+                    fence_proxy_async_smem();       // generic-proxy writes, read next by tcgen05.mma
+                    mbar_arrive(bar(sb, pk::Q_READY + buf));
+                }
+                ++uq;
+            }
+            if (more) nxt = finish_unit<kBC>(p, ahead, pairs, crank, smem);
+        }
     }
 
     tc_fence_before();
@@ -1599,8 +1719,9 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         for (const void* k : kernels)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        const void* persistent[2] = {(const void*)gen_attention_persistent_kernel<false>,
-                                     (const void*)gen_attention_persistent_kernel<true>};
+        const void* persistent[3] = {(const void*)gen_attention_persistent_kernel<false, false>,
+                                     (const void*)gen_attention_persistent_kernel<true, false>,
+                                     (const void*)gen_attention_persistent_kernel<false, true>};
         for (const void* k : persistent)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk::kSmemBytes);
@@ -1635,29 +1756,34 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     // computes and stores nothing of its own but still shares the K/V stream).
     const int qtiles = (N + tok_per_tile - 1) / tok_per_tile;
     const bool bc = mask_mode == NEO_MASK_BLOCK_CAUSAL;
-    if (!qn && (!bc || B == 1)) {
-        // Full mask, and the block-causal mask of one sequence (a prefill): the
-        // persistent kernel, one cluster per pair of SMs it can keep resident,
-        // each working through its share of the units.
+    if ((!qn && (!bc || B == 1)) || (qn && !bc)) {
+        // Full mask (with or without the folded query norm), and the
+        // block-causal mask of one sequence (a prefill): the persistent kernel,
+        // one cluster per pair of SMs it can keep resident, each working through
+        // its share of the units.
         static std::once_flag occ_once;
-        static int max_clusters = 0;
+        static int max_clusters_plain = 0, max_clusters_qn = 0;
         std::call_once(occ_once, [] {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = kCluster;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.gridDim = dim3(kCluster * 1024, 1, 1);
-            cfg.blockDim = dim3(kThreads, 1, 1);
-            cfg.dynamicSmemBytes = pk::kSmemBytes;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&max_clusters, (const void*)gen_attention_persistent_kernel<false>,
-                                               &cfg) != cudaSuccess)
-                max_clusters = 0;
-            cudaGetLastError();
+            for (int v = 0; v < 2; ++v) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr;
+                attr.id = cudaLaunchAttributeClusterDimension;
+                attr.val.clusterDim.x = kCluster;
+                attr.val.clusterDim.y = 1;
+                attr.val.clusterDim.z = 1;
+                cfg.gridDim = dim3(kCluster * 1024, 1, 1);
+                cfg.blockDim = dim3(v ? pk::kThreadsQN : kThreads, 1, 1);
+                cfg.dynamicSmemBytes = pk::kSmemBytes;
+                cfg.attrs = &attr;
+                cfg.numAttrs = 1;
+                int& mc = v ? max_clusters_qn : max_clusters_plain;
+                const void* k = v ? (const void*)gen_attention_persistent_kernel<false, true>
+                                  : (const void*)gen_attention_persistent_kernel<false, false>;
+                if (cudaOccupancyMaxActiveClusters(&mc, k, &cfg) != cudaSuccess) mc = 0;
+                cudaGetLastError();
+            }
         });
+        const int max_clusters = qn ? max_clusters_qn : max_clusters_plain;
         if (max_clusters < 1) return NEO_ERR_CUDA;
         const int pairs = (qtiles + kCluster - 1) / kCluster;
         const int64_t n_units = (int64_t)B * Hkv * pairs;
@@ -1667,15 +1793,15 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         // cluster in shared memory (at most pk::kMaxUnitsBC of them); beyond that
         // it takes the one-tile-per-CTA kernel below.
         if (!bc || (n_units + clusters - 1) / clusters <= pk::kMaxUnitsBC) {
-            // (both instantiations use the same threads and shared memory)
-            auto kernel = bc ? gen_attention_persistent_kernel<true> : gen_attention_persistent_kernel<false>;
-            kernel<<<dim3((unsigned)(clusters * kCluster)), kThreads, pk::kSmemBytes, stream>>>(
-                tq, to, tki, tvi, tkp, tvp, prm, (int)n_units, pairs);
+            auto kernel = qn ? gen_attention_persistent_kernel<false, true>
+                             : (bc ? gen_attention_persistent_kernel<true, false> : gen_attention_persistent_kernel<false, false>);
+            kernel<<<dim3((unsigned)(clusters * kCluster)), qn ? pk::kThreadsQN : kThreads, pk::kSmemBytes, stream>>>(
+                tq, to, tki, tvi, tkp, tvp, prm, (int)n_units, pairs, fr);
             return neo::launch_status();
         }
     }
-    // The folded query norm, and the block-causal mask of several sequences:
-    // one query tile per CTA.
+    // The block-causal mask of several sequences, with or without the folded
+    // query norm, and of one sequence with it: one query tile per CTA.
     const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
     auto kernel = bc ? (qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>)
                      : gen_attention_kernel<false, true>;

@@ -52,6 +52,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute the same count). dec gives registers back to the CTA's pool; inc
+// waits until the pool holds enough. Counts are multiples of 8 in [24, 256].
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// From the kLaunch registers a thread the kernel was launched with to kRegs:
+// inc above it, dec below it (dec to a count above the current one is not a
+// valid instruction), nothing when equal.
+template <int kRegs, int kLaunch>
+__device__ __forceinline__ void setmaxnreg_to() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg count");
+    if constexpr (kRegs > kLaunch) setmaxnreg_inc<kRegs>();
+    else if constexpr (kRegs < kLaunch) setmaxnreg_dec<kRegs>();
+}
+
 // True if the phase with the given parity has completed; never suspends the
 // thread (mbarrier.try_wait may, for a hardware-defined time).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {

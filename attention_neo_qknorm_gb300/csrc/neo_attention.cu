@@ -9,12 +9,13 @@
 // attention"): key j visible to query i iff T_j == T_i or j <= i.
 //
 // Two kernels share the roles below. gen_attention_persistent_kernel (the
-// full mask without the folded query norm) keeps one cluster per pair of SMs
-// resident and walks it through a sequence of query-tile pairs, so one
-// pair's epilogue overlaps the next pair's first tiles (its own comment,
-// further down, gives the hand-over). gen_attention_kernel (block-causal
-// mask and/or the query norm folded into the prologue) runs one query tile
-// per CTA.
+// full mask, with or without the query norm folded in, and the block-causal
+// mask of a single sequence) keeps one cluster per pair of SMs resident and
+// walks it through a sequence of query-tile pairs, so one pair's epilogue
+// overlaps the next pair's first tiles (its own comment, further down, gives
+// the hand-over). gen_attention_kernel (the block-causal mask of several
+// sequences, or of one with the folded query norm) runs one query tile per
+// CTA.
 //
 // Kernel shape (one CTA per 128-row query tile; D = 128; 12 warps; clusters
 // of two CTAs):
@@ -686,7 +687,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mx_tile[half * 128 + row] = pmax;
             }
             // The other half's maximum comes through shared memory; both warps
-            // of the pair leave this barrier with the same verdict.
+            // of the pair leave this barrier with the same outcome.
             // Both halves have read all of S_j into registers once they pass this
             // barrier, so either may then overwrite it with its part of P_j.
             tc_fence_before();
@@ -1469,7 +1470,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                         mx_tile[half * 128 + row] = pmax;
                     }
                     // The other half's maximum comes through shared memory; both warps of
-                    // the pair leave this barrier with the same verdict, and both have read
+                    // the pair leave this barrier with the same outcome, and both have read
                     // all of S into registers, so either may then overwrite it with P.
                     tc_fence_before();
                     ok = named_barrier_and(pair_bar, 64, ok);
@@ -1713,8 +1714,7 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         // (the full mask without the folded norm runs in the persistent kernel)
-        const void* kernels[3] = {(const void*)gen_attention_kernel<true, false>,
-                                  (const void*)gen_attention_kernel<false, true>,
+        const void* kernels[2] = {(const void*)gen_attention_kernel<true, false>,
                                   (const void*)gen_attention_kernel<true, true>};
         for (const void* k : kernels)
             if (attr_err == cudaSuccess)
@@ -1801,10 +1801,10 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         }
     }
     // The block-causal mask of several sequences, with or without the folded
-    // query norm, and of one sequence with it: one query tile per CTA.
+    // query norm, and of one sequence with it: one query tile per CTA (the
+    // full mask always returned above).
     const dim3 grid((unsigned)((qtiles + kCluster - 1) / kCluster * kCluster), (unsigned)Hkv, (unsigned)B);
-    auto kernel = bc ? (qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>)
-                     : gen_attention_kernel<false, true>;
+    auto kernel = qn ? gen_attention_kernel<true, true> : gen_attention_kernel<true, false>;
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, to, tki, tvi, tkp, tvp, fr, prm);
     return neo::launch_status();
 }

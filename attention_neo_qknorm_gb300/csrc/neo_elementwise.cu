@@ -549,7 +549,6 @@ rope2d_interleaved_kernel(T* __restrict__ x, int64_t n_tokens, int rows, int col
 // sequences before it, summed by the CTA (which also checks them).
 // ---------------------------------------------------------------------------
 constexpr int kCacheThreads = 128;
-constexpr int kCacheRows = 4;
 
 __global__ void __launch_bounds__(kCacheThreads)
 write_prefix_cache_kernel(const uint4* __restrict__ k_old, const uint4* __restrict__ v_old,
@@ -597,30 +596,16 @@ write_prefix_cache_kernel(const uint4* __restrict__ k_old, const uint4* __restri
         cu_out[b + 1] = (int32_t)(base + rows);
         if (b == 0) cu_out[0] = 0;
     }
-    // kCacheRows rows of a block in flight: all their loads before any store
-    // (no output overlaps an input the block reads; the host checks it).
-    const int64_t step = gridDim.x;
-    for (int64_t r0 = in_place ? old_rows + blockIdx.x : blockIdx.x; r0 < rows; r0 += step * kCacheRows) {
+    for (int64_t r = in_place ? old_rows + blockIdx.x : blockIdx.x; r < rows; r += gridDim.x) {
+        const bool old = r < old_rows;
+        const int64_t src = old ? (int64_t)lo + r : ((int64_t)b * N + (r - old_rows));
+        const uint4* ks = (old ? k_old : k_new) + src * row_u4;
+        const uint4* vs = (old ? v_old : v_new) + src * row_u4;
+        uint4* kd = k_out + (base + r) * row_u4;
+        uint4* vd = v_out + (base + r) * row_u4;
         for (int c = threadIdx.x; c < row_u4; c += kCacheThreads) {
-            uint4 kb[kCacheRows], vb[kCacheRows];
-#pragma unroll
-            for (int u = 0; u < kCacheRows; ++u) {
-                const int64_t r = r0 + u * step;
-                if (r < rows) {
-                    const bool old = r < old_rows;
-                    const int64_t src = old ? (int64_t)lo + r : ((int64_t)b * N + (r - old_rows));
-                    kb[u] = ((old ? k_old : k_new) + src * row_u4)[c];
-                    vb[u] = ((old ? v_old : v_new) + src * row_u4)[c];
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kCacheRows; ++u) {
-                const int64_t r = r0 + u * step;
-                if (r < rows) {
-                    k_out[(base + r) * row_u4 + c] = kb[u];
-                    v_out[(base + r) * row_u4 + c] = vb[u];
-                }
-            }
+            kd[c] = ks[c];
+            vd[c] = vs[c];
         }
     }
 }

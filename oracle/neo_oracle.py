@@ -1,7 +1,7 @@
 """fp64 CPU oracle of the NEO-unify generation-pass hot path.
 
-TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline leg
-of the benchmark may import this module. The CUDA library never calls it and
+TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU legs of the
+benchmark (its cpu_baseline and its reference arm) may import this module. The CUDA library never calls it and
 it shares no code with the CUDA library.
 
 Every function here is the plain definition of one step, written in float64

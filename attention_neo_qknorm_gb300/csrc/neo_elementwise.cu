@@ -170,7 +170,6 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
     constexpr int CHUNK_BYTES = kNormChunkRows * ROW_BYTES;
     static_assert(kNormChunkRows % RPW == 0, "a ring slot holds whole row groups");
 
-    __shared__ __align__(16) float w_s[2][128];   // norm weights of the full head dim: q, k
     extern __shared__ __align__(16) uint8_t ring_mem[];
 
     const int warp = threadIdx.x >> 5;
@@ -189,14 +188,6 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
         dim_a = 96 + m * E; half_w = 16; pair0 = 48 + m * E; axis = 2;
     }
     const int dim_b = dim_a + half_w;
-    for (int e = threadIdx.x; e < 256; e += kNormWarps * 32) {
-        const int which = e >> 7, d = e & 127;
-        const float* wt = which ? wk_t : wq_t;
-        const float* wh = which ? wk_hw : wq_hw;
-        const bool present = which ? Hkv > 0 : Hq > 0;
-        w_s[which][d] = present ? (d < 64 ? wt[d] : wh[d - 64]) : 0.f;
-    }
-    __syncthreads();
     const int64_t tok = (int64_t)blockIdx.x * kNormWarps + warp;
     if (tok >= S) return;
     // blockIdx.y picks the tensor: the q rows and the k rows of a token are
@@ -237,11 +228,14 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
     for (int j = 0; j < E; ++j) rope_sincos(pos, freqs.hi[pair0 + j], freqs.lo[pair0 + j], &sn[j], &cs[j]);
     float2 uc[P], vs[P], vc[P], us[P];
     auto fold = [&](int which) {
-        const float* w = w_s[which];
+        // The lane's dims lie in one normalised half: the temporal weights for
+        // [0,64), the height/width weights for [64,128). The weight loads come
+        // after the ring's copies are in flight.
+        const float* w = dim_a < 64 ? (which ? wk_t : wq_t) : (which ? wk_hw : wq_hw) - 64;
 #pragma unroll
         for (int i = 0; i < P; ++i) {
-            const float wu0 = w[dim_a + 2 * i], wu1 = w[dim_a + 2 * i + 1];
-            const float wv0 = w[dim_b + 2 * i], wv1 = w[dim_b + 2 * i + 1];
+            const float wu0 = __ldg(w + dim_a + 2 * i), wu1 = __ldg(w + dim_a + 2 * i + 1);
+            const float wv0 = __ldg(w + dim_b + 2 * i), wv1 = __ldg(w + dim_b + 2 * i + 1);
             uc[i] = make_float2(wu0 * cs[2 * i], wu1 * cs[2 * i + 1]);
             vs[i] = make_float2(-wv0 * sn[2 * i], -wv1 * sn[2 * i + 1]);
             vc[i] = make_float2(wv0 * cs[2 * i], wv1 * cs[2 * i + 1]);

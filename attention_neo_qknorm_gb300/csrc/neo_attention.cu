@@ -319,6 +319,14 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int qt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_kpre);
+        prefetch_tensormap(&tm_kimg);
+        prefetch_tensormap(&tm_vpre);
+        prefetch_tensormap(&tm_vimg);
+        prefetch_tensormap(&tm_o);
+    }
 
     // Prefix segment of this sequence; an inconsistent cu_prefix skips the CTA.
     const int lo = p.cu_prefix[b];
@@ -1043,6 +1051,17 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pk::kSmAbort);
     const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
 
+    // The tensor maps into the TMA unit's descriptor cache, by the lanes that
+    // issue the copies, while the barriers and TMEM are being set up.
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_kpre);
+        prefetch_tensormap(&tm_kimg);
+        prefetch_tensormap(&tm_o);
+    } else if (threadIdx.x == 2 * 32) {
+        prefetch_tensormap(&tm_vpre);
+        prefetch_tensormap(&tm_vimg);
+    }
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < pk::NUM_BARS; ++i) {
@@ -1108,8 +1127,9 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + pk::kSmTmemSlot);
     const uint32_t crank = cluster_ctarank();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 4 * 32) {
         // Report inconsistent prefix offsets once per CTA; such units are skipped by every role.
+        // A softmax thread does it: its first wait (for S) is longer than these loads.
         for (int U = cid; U < n_units; U += ncl)
             if (!decode<kBC>(p, U, pairs, crank, smem).ok) {
                 atomicOr(&g_dev_error, NEO_DEVERR_BAD_PREFIX);

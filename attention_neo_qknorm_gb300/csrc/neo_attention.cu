@@ -1050,6 +1050,9 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pk::kSmAbort);
     const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
+    // The first unit's prefix offsets, loaded now so that their latency passes
+    // during the set-up below.
+    const UnitLoad first = cid < n_units ? pk::load_unit(p, cid, pairs) : UnitLoad{0, 0, 0};
 
     // The tensor maps into the TMA unit's descriptor cache, by the lanes that
     // issue the copies, while the barriers and TMEM are being set up.
@@ -1189,7 +1192,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 q_issued = uqi;
                 return true;
             };
-            Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
+            Unit nxt = cid < n_units ? finish_unit<kBC>(p, first, pairs, crank, smem) : Unit{};
             for (int U = cid; ok && U < n_units; U += ncl) {
                 const Unit u = nxt;
                 const bool more = U + ncl < n_units;
@@ -1255,7 +1258,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         if (lane == 0) {
             bool ok = true;
             int gt = 0, uq = 0;
-            Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
+            Unit nxt = cid < n_units ? finish_unit<kBC>(p, first, pairs, crank, smem) : Unit{};
             for (int U = cid; ok && U < n_units; U += ncl) {
                 const Unit u = nxt;
                 const bool more = U + ncl < n_units;
@@ -1396,7 +1399,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             fence_proxy_async_smem();
             mbar_arrive(bar(sb, STAGED + e.buf));
         };
-        Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
+        Unit nxt = cid < n_units ? finish_unit<kBC>(p, first, pairs, crank, smem) : Unit{};
         for (int U = cid; U < n_units; U += ncl) {
             const Unit u = nxt;
             const bool more = U + ncl < n_units;
@@ -1562,7 +1565,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         const int64_t S = (int64_t)p.B * p.N;
         bool ok = true;
         int uq = 0;
-        Unit nxt = cid < n_units ? decode<kBC>(p, cid, pairs, crank, smem) : Unit{};
+        Unit nxt = cid < n_units ? finish_unit<kBC>(p, first, pairs, crank, smem) : Unit{};
         for (int U = cid; ok && U < n_units; U += ncl) {
             const Unit u = nxt;
             const bool more = U + ncl < n_units;

@@ -1050,10 +1050,6 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pk::kSmAbort);
     const BoundedWait wait{abort_flag, &g_dev_error, NEO_DEVERR_TIMEOUT, g_wait_limit_ns};
-    // The first unit's prefix offsets, loaded now so that their latency passes
-    // during the set-up below.
-    const UnitLoad first = cid < n_units ? pk::load_unit(p, cid, pairs) : UnitLoad{0, 0, 0};
-
     // The tensor maps into the TMA unit's descriptor cache, by the lanes that
     // issue the copies, while the barriers and TMEM are being set up.
     if (threadIdx.x == 0) {
@@ -1083,6 +1079,10 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         tmem_alloc(sb + pk::kSmTmemSlot, kTmCols);
         tmem_relinquish();
     }
+    // Everything above touches only this CTA's own resources and may overlap the
+    // previous kernel of the stream; global memory is read after this wait.
+    griddep_wait();
+    const UnitLoad first = cid < n_units ? pk::load_unit(p, cid, pairs) : UnitLoad{0, 0, 0};
     const int n_img = (p.N + kBlockN - 1) / kBlockN;
     if constexpr (kBC) {
         // One warp per image tile: the temporal-index range of each 64-key half
@@ -1818,9 +1818,9 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         if (!bc || (n_units + clusters - 1) / clusters <= pk::kMaxUnitsBC) {
             auto kernel = qn ? gen_attention_persistent_kernel<false, true>
                              : (bc ? gen_attention_persistent_kernel<true, false> : gen_attention_persistent_kernel<false, false>);
-            kernel<<<dim3((unsigned)(clusters * kCluster)), qn ? pk::kThreadsQN : kThreads, pk::kSmemBytes, stream>>>(
-                tq, to, tki, tvi, tkp, tvp, prm, (int)n_units, pairs, fr);
-            return neo::launch_status();
+            return neo::launch_overlapped(kernel, dim3((unsigned)(clusters * kCluster)),
+                                          dim3(qn ? pk::kThreadsQN : kThreads), pk::kSmemBytes, stream, tq, to, tki,
+                                          tvi, tkp, tvp, prm, (int)n_units, pairs, fr);
         }
     }
     // The block-causal mask of several sequences, with or without the folded

@@ -217,6 +217,9 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
         }
         asm volatile("cp.async.commit_group;" ::: "memory");   // possibly empty: keeps the group count uniform
     };
+    // The attention launched after this kernel may start setting up its CTAs
+    // now; it waits for this grid to complete before it reads q and k.
+    sm103::griddep_launch_dependents();
 #pragma unroll
     for (int c = 0; c < kNormDepth; ++c) issue(c);
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "neo.h"
@@ -13,6 +14,30 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline neo_status launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? NEO_OK : NEO_ERR_CUDA;
+}
+
+// Launches `kernel` on `stream` allowing it to start while the previous kernel
+// of the stream finishes (programmatic stream serialization); the kernel waits
+// (griddepcontrol.wait) before its first global memory access.
+template <typename... Params, typename... Args>
+inline neo_status launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return NEO_ERR_CUDA;
+    }
+    return launch_status();
 }
 
 // Attention translation unit: device error word and wait limit.

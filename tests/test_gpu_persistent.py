@@ -75,3 +75,37 @@ def test_many_short_sequences(gpu_lib):
     assert_bf16_close(take_rows(f64(out.cpu()), rows), ref, "1100 sequences")
     got_lse = np.array([f64(lse.cpu())[b, h, n] for b, n, h in rows])
     np.testing.assert_allclose(got_lse, ref_lse, rtol=1e-3, atol=2e-2)
+
+
+def test_norm_then_attention_back_to_back(gpu_lib):
+    """The attention is launched so that its CTAs may start while the QK-norm
+    kernel before it drains; it must still read the normed q and k. Ten rounds
+    over fresh raw inputs, norm and attention back to back in one stream, give
+    the same bits as the same rounds with a device synchronisation between the
+    two launches."""
+    w = synth.small_workload(prefix=(700, 300), grid=(24, 24), Hq=32, Hkv=8, B=2)
+    layer = GpuLayer(w, synth.make_inputs(w, seed=41))
+    g = torch.Generator(device="cuda").manual_seed(42)
+    raws = [(torch.randn(layer.q.shape, device="cuda", generator=g).to(torch.bfloat16),
+             torch.randn(layer.k.shape, device="cuda", generator=g).to(torch.bfloat16)) for _ in range(10)]
+
+    def rounds(sync):
+        outs = []
+        for q_raw, k_raw in raws:
+            layer.q.copy_(q_raw)
+            layer.k.copy_(k_raw)
+            layer.norm_rope()
+            if sync:
+                torch.cuda.synchronize()
+            layer.attention()
+            outs.append((layer.out.clone(), layer.lse.clone()))
+        torch.cuda.synchronize()
+        return outs
+
+    serial = rounds(True)
+    overlapped = rounds(False)
+    check_device_ok()
+    for (a, la), (b, lb) in zip(serial, overlapped):
+        assert torch.equal(a, b) and torch.equal(la, lb)
+    # and the rounds differ from one another (the inputs changed)
+    assert not torch.equal(serial[0][0], serial[1][0])

@@ -77,27 +77,45 @@ def test_many_short_sequences(gpu_lib):
     np.testing.assert_allclose(got_lse, ref_lse, rtol=1e-3, atol=2e-2)
 
 
-def test_norm_then_attention_back_to_back(gpu_lib):
+@pytest.mark.parametrize("mode", ["full", "folded", "prefill"])
+def test_norm_then_attention_back_to_back(gpu_lib, mode):
     """The attention is launched so that its CTAs may start while the QK-norm
     kernel before it drains; it must still read the normed q and k. Ten rounds
     over fresh raw inputs, norm and attention back to back in one stream, give
     the same bits as the same rounds with a device synchronisation between the
-    two launches."""
-    w = synth.small_workload(prefix=(700, 300), grid=(24, 24), Hq=32, Hkv=8, B=2)
+    two launches: the full mask, the query norm folded into the attention (the
+    keys' norm before it), and a one-sequence block-causal prefill."""
+    if mode == "prefill":
+        w = synth.small_workload(prefix=(0,), grid=(30, 30), Hq=32, Hkv=8, B=1)
+    else:
+        w = synth.small_workload(prefix=(700, 300), grid=(24, 24), Hq=32, Hkv=8, B=2)
     layer = GpuLayer(w, synth.make_inputs(w, seed=41))
     g = torch.Generator(device="cuda").manual_seed(42)
     raws = [(torch.randn(layer.q.shape, device="cuda", generator=g).to(torch.bfloat16),
              torch.randn(layer.k.shape, device="cuda", generator=g).to(torch.bfloat16)) for _ in range(10)]
+    # A prefill: text-like temporal indexes, runs of 40 tokens sharing one.
+    t_img = (torch.arange(w.N, dtype=torch.int32, device="cuda") // 40).contiguous()
 
     def rounds(sync):
         outs = []
         for q_raw, k_raw in raws:
             layer.q.copy_(q_raw)
             layer.k.copy_(k_raw)
-            layer.norm_rope()
+            if mode == "folded":
+                layer.norm_rope_k()
+            else:
+                layer.norm_rope()
             if sync:
                 torch.cuda.synchronize()
-            layer.attention()
+            if mode == "folded":
+                layer.attention_qnorm()
+            elif mode == "prefill":
+                neo.neo_gen_attention(layer.q.view(1, w.N, w.Hq, w.D), None, None,
+                                      layer.k.view(1, w.N, w.Hkv, w.D), layer.v, layer.cu, 0, layer.out,
+                                      scale=SCALE, lse=layer.lse, mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
+                                      t_img=t_img)
+            else:
+                layer.attention()
             outs.append((layer.out.clone(), layer.lse.clone()))
         torch.cuda.synchronize()
         return outs

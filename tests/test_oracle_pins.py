@@ -278,6 +278,32 @@ def test_block_causal_with_distinct_indices_is_plain_causal():
     np.testing.assert_allclose(out[0], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
 
 
+def test_block_causal_visible_sets_with_temporal_indexes_out_of_order():
+    """Hand-checked visible sets of the block-causal rule with temporal indexes
+    that are not in order ("SenseNova-U1.5" §Block-causal attention: tokens
+    that share a temporal index see each other both ways; across differing
+    indexes ordinary causality holds). Prefix of two keys (T = 0, 1), image
+    segment of four tokens (T = 4, 2, 4, 3), so over the concatenated order
+    T = [0, 1, 4, 2, 4, 3]. With scale 0 every visible key gets the same
+    weight, and one-hot values make the output the indicator of the visible
+    set divided by its size. A rule of T_j <= T_i would let query 2 (T = 4)
+    see keys 3 and 5 and hide key 2 from query 3 (T = 2)."""
+    D = 128
+    g = np.random.default_rng(31)
+    q = g.standard_normal((1, 4, 1, D))
+    kp, ki = g.standard_normal((2, 1, D)), g.standard_normal((1, 4, 1, D))
+    eye = np.eye(D)
+    vp = eye[:2].reshape(2, 1, D)
+    vi = eye[2:6].reshape(1, 4, 1, D)
+    out, _ = O.gen_attention(q, kp, vp, ki, vi, np.array([0, 2]), 0.0, mask_mode=O.MASK_BLOCK_CAUSAL,
+                             t_prefix=np.array([0, 1]), t_img=np.array([[4, 2, 4, 3]]))
+    visible = {0: [0, 1, 2, 4], 1: [0, 1, 2, 3], 2: [0, 1, 2, 3, 4], 3: [0, 1, 2, 3, 4, 5]}
+    for n, keys in visible.items():
+        want = np.zeros(D)
+        want[keys] = 1.0 / len(keys)
+        np.testing.assert_allclose(out[0, n, 0], want, rtol=0, atol=1e-15, err_msg=f"query {n}")
+
+
 def test_attention_sampled_rows_match_full():
     q, kp, vp, ki, vi, cu = _attn_case(B=2, Ls=(7, 2), N=6, Hq=4, Hkv=2, seed=25)
     full, full_lse = O.gen_attention(q, kp, vp, ki, vi, cu, 0.3)
@@ -382,6 +408,63 @@ def test_cfg_dual_reduces_to_the_two_scale_branches():
     zs, _, _ = O.flow_cfg_euler_step(z, c, c, c, t, t + 0.1, 3.0, 1.7)
     ze, _ = O.flow_euler_step(z, c, t, t + 0.1)
     np.testing.assert_allclose(zs, ze, rtol=1e-12, atol=1e-12)
+
+
+def test_cfg_branches_on_a_hand_worked_example():
+    """The four branch formulas of the inference loop ("SenseNova-U1" §2.7),
+    worked by hand: z = 0, t = 0.5 (so each v_X = 2 x0_X), t_next = 0.6,
+    x0 = 1 (cond), 0.5 (text-unconditional), 0 (unconditional) give
+    v_c = 2, v_tu = 1, v_u = 0."""
+    z, c, tu, u = (np.zeros(3), np.ones(3), np.full(3, 0.5), np.zeros(3))
+    cases = [  # (g, g_img, branch, v)
+        (1.0, 1.0, O.CFG_NONE, 2.0),      # v_c
+        (4.0, 1.0, O.CFG_TEXT, 5.0),      # v_tu + 4 (v_c - v_tu) = 1 + 4
+        (3.0, 3.0, O.CFG_CLASSIC, 6.0),   # v_u + 3 (v_c - v_u) = 0 + 6
+        (4.0, 1.5, O.CFG_DUAL, 5.5),      # v_u + 4 (v_c - v_tu) + 1.5 (v_tu - v_u) = 4 + 1.5
+    ]
+    for g, gi, branch, v in cases:
+        zn, vv, br = O.flow_cfg_euler_step(z, c, tu, u, 0.5, 0.6, g, gi)
+        assert br == branch
+        np.testing.assert_allclose(vv, v, rtol=1e-15)
+        np.testing.assert_allclose(zn, 0.1 * v, rtol=1e-14)
+
+
+def test_cfg_classic_is_cond_against_the_full_unconditional():
+    """The classic branch is single-axis guidance of cond against the fully
+    unconditional prediction, (1 - g) v_u + g v_c ("SenseNova-U1" §2.7); it
+    reads no text-unconditional prediction (NaN there changes nothing), and
+    the text branch reads no unconditional one. Velocities come from the
+    plain Euler step of each prediction."""
+    z, c, tu, u = _cfg_inputs(seed=43)
+    t, g = 0.35, 3.0
+    nan = np.full_like(z, np.nan)
+    zn, v, br = O.flow_cfg_euler_step(z, c, nan, u, t, t + 0.1, g, g)
+    assert br == O.CFG_CLASSIC
+    _, vc = O.flow_euler_step(z, c, t, t + 0.1)
+    _, vu = O.flow_euler_step(z, u, t, t + 0.1)
+    np.testing.assert_allclose(v, (1 - g) * vu + g * vc, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(zn, z + 0.1 * v, rtol=1e-12, atol=1e-12)
+    _, vt, br = O.flow_cfg_euler_step(z, c, tu, nan, t, t + 0.1, g, 1.0)
+    assert br == O.CFG_TEXT and np.all(np.isfinite(vt))
+
+
+def test_cfg_dual_meets_the_text_and_classic_branches():
+    """The dual form is affine in img_cfg_scale with slope v_tu - v_u, and it
+    equals the text branch at img scale 1 and the classic branch at equal
+    scales ("SenseNova-U1" §2.7, Eq. 6 and its two reductions). Both sides are
+    oracle calls: the dual branch just off each meeting point against the
+    branch the loop takes at that point."""
+    z, c, tu, u = _cfg_inputs(seed=44)
+    t, g, d = 0.25, 3.0, 0.5
+    _, vtu = O.flow_euler_step(z, tu, t, t + 0.1)
+    _, vu = O.flow_euler_step(z, u, t, t + 0.1)
+    _, v_text, b_text = O.flow_cfg_euler_step(z, c, tu, u, t, t + 0.1, g, 1.0)
+    _, v_cls, b_cls = O.flow_cfg_euler_step(z, c, tu, u, t, t + 0.1, g, g)
+    _, v_d1, b_d1 = O.flow_cfg_euler_step(z, c, tu, u, t, t + 0.1, g, 1.0 + d)
+    _, v_d2, b_d2 = O.flow_cfg_euler_step(z, c, tu, u, t, t + 0.1, g, g + d)
+    assert (b_text, b_cls, b_d1, b_d2) == (O.CFG_TEXT, O.CFG_CLASSIC, O.CFG_DUAL, O.CFG_DUAL)
+    np.testing.assert_allclose(v_d1 - v_text, d * (vtu - vu), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(v_d2 - v_cls, d * (vtu - vu), rtol=1e-11, atol=1e-11)
 
 
 # ---------------------------------------------------------------- sampler pieces

@@ -1,15 +1,16 @@
 """End-to-end parity of one generation-pass layer (positions -> QK-norm +
 three-axis RoPE -> attention over prefix + image keys) on the five workloads,
 in the launch configurations the benchmark times (query norm in place before
-the attention, or folded into it). Small workloads are compared
-element by element; the full-size ones on sampled query rows that the oracle
-computes one by one."""
+the attention, or folded into it), element by element over every output row
+at full size; and each workload's Euler step on its whole z."""
 
 import numpy as np
 import pytest
+import torch
 
-from attention_neo_qknorm_gb300 import synth
-from helpers import GpuLayer, assert_bf16_close, f64, oracle_layer, take_rows
+import oracle as O
+from attention_neo_qknorm_gb300 import neo, synth
+from helpers import F32_TOL, GpuLayer, assert_bf16_close, f64, max_abs, oracle_layer, rel_frob
 
 pytestmark = pytest.mark.gpu
 
@@ -36,18 +37,32 @@ def test_small_workload_full_compare(gpu_lib, fused):
     np.testing.assert_allclose(f64(layer.lse), ref_lse, rtol=1e-3, atol=2e-2)
 
 
-@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
-def test_workload_layer_matches_oracle(gpu_lib, name, fused):
+def test_workload_layer_matches_oracle(gpu_lib, name):
+    """Every output row and every log-sum-exp of the workload, both launch
+    configurations, against one oracle computation of the whole layer."""
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w)
-    layer = GpuLayer(w, inp)
-    run_layer(layer, fused)
-    if w.B * w.N * w.Hq <= 4096:
-        ref, _ = oracle_layer(w, inp)
-        assert_bf16_close(f64(layer.out), ref, name)
-    else:
-        rows = synth.random_rows(w, 384, seed=5)
-        ref, _ = oracle_layer(w, inp, rows=rows)
-        got = take_rows(f64(layer.out), rows)
-        assert_bf16_close(got, ref, name + " (sampled rows)")
+    ref, ref_lse = oracle_layer(w, inp)
+    for fused in (False, True):
+        layer = GpuLayer(w, inp)
+        run_layer(layer, fused)
+        tag = f"{name} ({'folded query norm' if fused else 'norm then attention'}, all rows)"
+        assert_bf16_close(f64(layer.out), ref, tag)
+        np.testing.assert_allclose(f64(layer.lse), ref_lse, rtol=1e-3, atol=2e-2, err_msg=tag)
+        del layer
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_workload_euler_step_matches_oracle(gpu_lib, name):
+    """The workload's Euler step on its whole z (B*N x 3072 fp32), with the
+    velocity written out, at its first flow time."""
+    w = synth.WORKLOADS[name]
+    z, (x0,) = synth.make_flow(w)
+    t, tn = w.t_steps[0], w.t_steps[0] + w.dt
+    zd, xd = z.cuda(), x0.cuda()
+    vd = torch.empty_like(zd)
+    neo.neo_flow_euler_step(zd, xd, t, tn, 0.02, vd)
+    rz, rv = O.flow_euler_step(f64(z), f64(x0), np.float32(t), np.float32(tn), np.float32(0.02))
+    assert max_abs(f64(zd), rz) <= F32_TOL * max(1.0, float(np.abs(rz).max()))
+    assert rel_frob(f64(zd), rz) <= F32_TOL and rel_frob(f64(vd), rv) <= F32_TOL

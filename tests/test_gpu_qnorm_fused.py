@@ -97,3 +97,23 @@ def test_fused_rejects_missing_parameters(gpu_lib):
         with pytest.raises(neo.NeoError) as e:
             neo.neo_gen_attention_qnorm(q, None, None, k, k, cu, 0, q.clone(), idx, w, w, **kw)
         assert e.value.status == neo.NEO_ERR_INVALID_ARG
+
+
+def test_fused_equals_two_launches_at_large_positions(gpu_lib):
+    """Positions up to 2^30 on every axis: the folded prologue and the
+    standalone kernel reduce the angles the same way, so the bits agree."""
+    S, Hq, Hkv = 200, 8, 2
+    g = torch.Generator().manual_seed(6)
+    q = torch.randn(1, S, Hq, 128, generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(1, S, Hkv, 128, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(1, S, Hkv, 128, generator=g).to(torch.bfloat16).cuda()
+    ws = [(torch.rand(64, generator=g) + 0.5).cuda() for _ in range(2)]
+    idx = torch.randint(0, 1 << 30, (3, S), generator=g, dtype=torch.int32).cuda()
+    cu = torch.zeros(2, dtype=torch.int32, device="cuda")
+    fused = torch.empty_like(q)
+    neo.neo_gen_attention_qnorm(q, None, None, k, v, cu, 0, fused, idx, ws[0], ws[1])
+    qn = q.clone().reshape(S, Hq, 128)
+    neo.neo_qknorm_rope3(qn, None, idx, ws[0], ws[1], None, None)
+    plain = torch.empty_like(q)
+    neo.neo_gen_attention(qn.view(1, S, Hq, 128), None, None, k, v, cu, 0, plain)
+    assert torch.equal(fused, plain)

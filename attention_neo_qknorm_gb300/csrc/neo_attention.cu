@@ -161,15 +161,14 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, int i) { return sba
 // below (chunk pair s, element pair j -> index 8 s + j). They depend only on
 // the token's positions, so they are computed while the Q tile is in flight.
 template <int half>
-__device__ __forceinline__ void qnorm_rope_angles(const float pos[3], const neo::RopeFreqs& fr, float (&cs)[32],
+__device__ __forceinline__ void qnorm_rope_angles(const int32_t pos[3], const neo::RopeFreqs& fr, float (&cs)[32],
                                                   float (&sn)[32]) {
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int pair0 = half ? (s < 2 ? 32 + 8 * s : 48 + 8 * (s - 2)) : 8 * s;
-        const float p_s = pos[half ? (s < 2 ? 1 : 2) : 0];
+        const int32_t p_s = pos[half ? (s < 2 ? 1 : 2) : 0];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            neo::rope_sincos(p_s, fr.hi[pair0 + j], fr.lo[pair0 + j], &sn[8 * s + j], &cs[8 * s + j]);
+        for (int j = 0; j < 8; ++j) neo::rope_sincos(p_s, fr.turn[pair0 + j], &sn[8 * s + j], &cs[8 * s + j]);
     }
 }
 
@@ -247,7 +246,7 @@ __device__ __forceinline__ void qnorm_rope_q_half(uint8_t* half_tile, int row, c
 // in registers: the same calls and operations on the same values (hence the
 // same bits) in fewer registers.
 template <int half>
-__device__ __forceinline__ void qnorm_rope_q_half_lowreg(uint8_t* half_tile, int row, const float pos[3],
+__device__ __forceinline__ void qnorm_rope_q_half_lowreg(uint8_t* half_tile, int row, const int32_t pos[3],
                                                          const neo::RopeFreqs& fr, const float* w, float eps) {
     uint8_t* rowp = half_tile + row * 128;
     auto chunk = [&](int c) { return *reinterpret_cast<const uint4*>(rowp + ((c ^ (row & 7)) << 4)); };
@@ -275,10 +274,10 @@ __device__ __forceinline__ void qnorm_rope_q_half_lowreg(uint8_t* half_tile, int
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int pair0 = half ? (s < 2 ? 32 + 8 * s : 48 + 8 * (s - 2)) : 8 * s;
-        const float p_s = pos[half ? (s < 2 ? 1 : 2) : 0];
+        const int32_t p_s = pos[half ? (s < 2 ? 1 : 2) : 0];
         float cs[8], sn[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) neo::rope_sincos(p_s, fr.hi[pair0 + j], fr.lo[pair0 + j], &sn[j], &cs[j]);
+        for (int j = 0; j < 8; ++j) neo::rope_sincos(p_s, fr.turn[pair0 + j], &sn[j], &cs[j]);
         float2 xa[4], xb[4];
         unpack(chunk(pa[s]), xa);   // not yet written: chunk pairs are disjoint
         unpack(chunk(pb[s]), xb);
@@ -589,9 +588,9 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             float* w_s = reinterpret_cast<float*>(smem + kSmQnW);
             if (t < 128) w_s[t] = t < 64 ? __ldg(p.qn_w_t + t) : __ldg(p.qn_w_hw + (t - 64));
             const int64_t tok = (int64_t)b * p.N + min(n0 + qrow / p.G, p.N - 1);
-            float pos[3];
+            int32_t pos[3];
 #pragma unroll
-            for (int a = 0; a < 3; ++a) pos[a] = (float)__ldg(p.qn_idx + a * S + tok);
+            for (int a = 0; a < 3; ++a) pos[a] = __ldg(p.qn_idx + a * S + tok);
             float cs[32], sn[32];
             if (qhalf == 0)   // warp-uniform
                 qnorm_rope_angles<0>(pos, qn_freqs, cs, sn);
@@ -1574,9 +1573,9 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 const int buf = uq & 1;
                 uint8_t* sQ = smem + kSmQ0 + (uint32_t)buf * kTile;
                 const int64_t tok = (int64_t)u.b * p.N + min(u.n0 + t / p.G, p.N - 1);
-                float pos[3];
+                int32_t pos[3];
 #pragma unroll
-                for (int a = 0; a < 3; ++a) pos[a] = (float)__ldg(p.qn_idx + a * S + tok);
+                for (int a = 0; a < 3; ++a) pos[a] = __ldg(p.qn_idx + a * S + tok);
                 ok = __all_sync(0xffffffffu, wait(bar(sb, Q_FULL + buf), (uint32_t)(uq >> 1) & 1u));
                 if (ok) {
                     qnorm_rope_q_half_lowreg<0>(sQ, t, pos, qn_freqs, w_s, p.qn_eps);
@@ -1733,23 +1732,24 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
             return NEO_ERR_CUDA;
     }
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
+    static neo::DeviceOnce attr_slots[neo::kMaxDevices];
+    neo::DeviceOnce* attr = neo::device_slot(attr_slots);
+    if (!attr) return NEO_ERR_CUDA;
+    std::call_once(attr->once, [attr] {
         // (the full mask without the folded norm runs in the persistent kernel)
         const void* kernels[2] = {(const void*)gen_attention_kernel<true, false>,
                                   (const void*)gen_attention_kernel<true, true>};
         for (const void* k : kernels)
-            if (attr_err == cudaSuccess)
-                attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (attr->err == cudaSuccess)
+                attr->err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         const void* persistent[3] = {(const void*)gen_attention_persistent_kernel<false, false>,
                                      (const void*)gen_attention_persistent_kernel<true, false>,
                                      (const void*)gen_attention_persistent_kernel<false, true>};
         for (const void* k : persistent)
-            if (attr_err == cudaSuccess)
-                attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk::kSmemBytes);
+            if (attr->err == cudaSuccess)
+                attr->err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pk::kSmemBytes);
     });
-    if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
+    if (attr->err != cudaSuccess) return NEO_ERR_CUDA;
 
     AttnParams prm;
     prm.cu_prefix = cu_prefix;
@@ -1784,9 +1784,12 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
         // block-causal mask of one sequence (a prefill): the persistent kernel,
         // one cluster per pair of SMs it can keep resident, each working through
         // its share of the units.
-        static std::once_flag occ_once;
-        static int max_clusters_plain = 0, max_clusters_qn = 0;
-        std::call_once(occ_once, [] {
+        // Clusters the device keeps resident, per variant (plain, folded norm),
+        // found once per device after the attributes above are set.
+        static neo::DeviceOnce occ_slots[neo::kMaxDevices];
+        neo::DeviceOnce* occ = neo::device_slot(occ_slots);
+        if (!occ) return NEO_ERR_CUDA;
+        std::call_once(occ->once, [occ] {
             for (int v = 0; v < 2; ++v) {
                 cudaLaunchConfig_t cfg = {};
                 cudaLaunchAttribute attr;
@@ -1799,14 +1802,14 @@ neo_status launch_attention(const void* q_img, const void* k_prefix, const void*
                 cfg.dynamicSmemBytes = pk::kSmemBytes;
                 cfg.attrs = &attr;
                 cfg.numAttrs = 1;
-                int& mc = v ? max_clusters_qn : max_clusters_plain;
+                int& mc = occ->value[v];
                 const void* k = v ? (const void*)gen_attention_persistent_kernel<false, true>
                                   : (const void*)gen_attention_persistent_kernel<false, false>;
                 if (cudaOccupancyMaxActiveClusters(&mc, k, &cfg) != cudaSuccess) mc = 0;
                 cudaGetLastError();
             }
         });
-        const int max_clusters = qn ? max_clusters_qn : max_clusters_plain;
+        const int max_clusters = occ->value[qn ? 1 : 0];
         if (max_clusters < 1) return NEO_ERR_CUDA;
         const int pairs = (qtiles + kCluster - 1) / kCluster;
         const int64_t n_units = (int64_t)B * Hkv * pairs;

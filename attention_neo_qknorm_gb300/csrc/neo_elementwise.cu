@@ -25,15 +25,19 @@ namespace {
 using neo::RopeFreqs;
 using neo::rope_sincos;
 
+// The current device's SM count (looked up once per device).
 int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
+    static neo::DeviceOnce slots[neo::kMaxDevices];
+    neo::DeviceOnce* s = neo::device_slot(slots);
+    if (!s) return 152;
+    std::call_once(s->once, [s] {
+        int dev = 0, n = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-    }
-    return n;
+            n = 152;
+        s->value[0] = n;
+    });
+    return s->value[0];
 }
 
 // ---------------------------------------------------------------------------
@@ -225,10 +229,10 @@ qknorm_rope3_kernel(T* __restrict__ q, T* __restrict__ k, int64_t S, int Hq, int
 
     // The token's angles for this lane's pairs, and the weight-folded products
     // (w_u cos, -w_v sin) for u' and (w_v cos, w_u sin) for v', element pairs packed.
-    const float pos = (float)__ldg(idx + axis * S + tok);
+    const int32_t pos = __ldg(idx + axis * S + tok);
     float cs[E], sn[E];
 #pragma unroll
-    for (int j = 0; j < E; ++j) rope_sincos(pos, freqs.hi[pair0 + j], freqs.lo[pair0 + j], &sn[j], &cs[j]);
+    for (int j = 0; j < E; ++j) rope_sincos(pos, freqs.turn[pair0 + j], &sn[j], &cs[j]);
     float2 uc[P], vs[P], vc[P], us[P];
     auto fold = [&](int which) {
         // The lane's dims lie in one normalised half: the temporal weights for
@@ -517,7 +521,7 @@ rope2d_interleaved_kernel(T* __restrict__ x, int64_t n_tokens, int rows, int col
 #pragma unroll
                     for (int k = 0; k < kPairs; ++k) {
                         float sn, cs;
-                        rope_sincos((float)(by_row[k] ? r : c), fh[k], 0.f, &sn, &cs);
+                        neo::rope_sincos_small((float)(by_row[k] ? r : c), fh[k], &sn, &cs);
                         o[2 * k] = fmaf(v[u][2 * k], cs, -v[u][2 * k + 1] * sn);
                         o[2 * k + 1] = fmaf(v[u][2 * k + 1], cs, v[u][2 * k] * sn);
                     }
@@ -674,23 +678,26 @@ extern "C" neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype, int64_
         return NEO_ERR_INVALID_ARG;
     if (S == 0 || Hq + Hkv == 0) return NEO_OK;
     if (!indexes) return NEO_ERR_INVALID_ARG;
+    const int64_t esz = dtype == NEO_BF16 ? 2 : 4;
+    if (Hq > 0 && Hkv > 0 && neo::overlap(q, S * Hq * 128 * esz, k, S * Hkv * 128 * esz)) return NEO_ERR_INVALID_ARG;
 
     const RopeFreqs fr = neo::rope3_freqs(theta_t, theta_hw);
     const int64_t blocks = (S + kNormWarps - 1) / kNormWarps;
     if (blocks > INT32_MAX) return NEO_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)blocks, (Hq > 0 ? 1u : 0u) + (Hkv > 0 ? 1u : 0u));
     const size_t ring = (size_t)kNormWarps * kNormDepth * kNormChunkRows * 128 * (dtype == NEO_BF16 ? 2 : 4);
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
+    static neo::DeviceOnce attr_slots[neo::kMaxDevices];
+    neo::DeviceOnce* attr = neo::device_slot(attr_slots);
+    if (!attr) return NEO_ERR_CUDA;
+    std::call_once(attr->once, [attr] {
         const int bytes = 96 * 1024;
-        attr_err = cudaFuncSetAttribute(qknorm_rope3_kernel<__nv_bfloat16>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(qknorm_rope3_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            bytes);
+        attr->err = cudaFuncSetAttribute(qknorm_rope3_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (attr->err == cudaSuccess)
+            attr->err = cudaFuncSetAttribute(qknorm_rope3_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             bytes);
     });
-    if (attr_err != cudaSuccess) return NEO_ERR_CUDA;
+    if (attr->err != cudaSuccess) return NEO_ERR_CUDA;
     if (dtype == NEO_BF16) {
         qknorm_rope3_kernel<__nv_bfloat16><<<grid, kNormWarps * 32, ring, stream>>>(
             static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), S, Hq, Hkv, indexes, q_norm_w,
@@ -711,6 +718,10 @@ extern "C" neo_status neo_flow_euler_step(float* z, const float* x0_hat, int64_t
     if (n == 0) return NEO_OK;
     if (!z || !x0_hat || !neo::aligned16(z) || !neo::aligned16(x0_hat)) return NEO_ERR_INVALID_ARG;
     if (v_out && !neo::aligned16(v_out)) return NEO_ERR_INVALID_ARG;
+    // The kernel reads z and x0_hat once and writes z and v_out: no overlaps.
+    const int64_t nb = n * 4;
+    if (neo::overlap(z, nb, x0_hat, nb) || neo::overlap(v_out, nb, z, nb) || neo::overlap(v_out, nb, x0_hat, nb))
+        return NEO_ERR_INVALID_ARG;
     const float den = std::fmax(1.0f - t, t_eps);
     if (!(den > 0.f)) return NEO_ERR_INVALID_ARG;
     const float dt = t_next - t;
@@ -757,6 +768,15 @@ extern "C" neo_status neo_flow_cfg_euler_step(float* z, const float* x0_cond, co
     if (!neo::aligned16(z) || !neo::aligned16(xa) || (xb && !neo::aligned16(xb)) || (xc && !neo::aligned16(xc)) ||
         (v_out && !neo::aligned16(v_out)))
         return NEO_ERR_INVALID_ARG;
+    // Predictions are only read and may share a buffer; z and v_out are
+    // written, so neither may overlap anything the kernel reads, nor each other.
+    {
+        const int64_t nb = n * 4;
+        const void* reads[3] = {xa, K > 1 ? xb : nullptr, K > 2 ? xc : nullptr};
+        for (const void* r : reads)
+            if (neo::overlap(z, nb, r, nb) || neo::overlap(v_out, nb, r, nb)) return NEO_ERR_INVALID_ARG;
+        if (neo::overlap(v_out, nb, z, nb)) return NEO_ERR_INVALID_ARG;
+    }
     const float den = std::fmax(1.0f - t, t_eps);
     if (!(den > 0.f)) return NEO_ERR_INVALID_ARG;
     const float dt = t_next - t;
@@ -828,11 +848,7 @@ extern "C" neo_status neo_write_prefix_cache(const void* k_old, const void* v_ol
     // The outputs may not overlap any input, except the in-place append of a
     // single sequence (k_out == k_old and v_out == v_old).
     const bool in_place = B == 1 && k_out == k_old && v_out == v_old && total_old > 0;
-    auto overlap = [](const void* a, int64_t an, const void* b, int64_t bn) {
-        if (!a || !b || an <= 0 || bn <= 0) return false;
-        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-        return a0 < b0 + (uintptr_t)bn && b0 < a0 + (uintptr_t)an;
-    };
+    using neo::overlap;
     const int64_t out_bytes = capacity * row, old_bytes = total_old * row, new_bytes = (int64_t)B * N * row;
     const void* outs[2] = {k_out, v_out};
     for (const void* o : outs) {

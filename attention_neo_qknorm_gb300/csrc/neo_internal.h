@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <utility>
 #include <cuda_runtime.h>
 
@@ -10,6 +11,32 @@
 namespace neo {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether the byte ranges [a, a + an) and [b, b + bn) share a byte (a null
+// pointer or an empty range overlaps nothing).
+inline bool overlap(const void* a, int64_t an, const void* b, int64_t bn) {
+    if (!a || !b || an <= 0 || bn <= 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + (uintptr_t)bn && y < x + (uintptr_t)an;
+}
+
+// Host state that is set up once per device (kernel attributes, sizes
+// derived from occupancy): one slot per device ordinal, filled the first time
+// the library is called with that device current.
+constexpr int kMaxDevices = 64;
+
+struct DeviceOnce {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int value[2] = {0, 0};
+};
+
+// The current device's slot of `slots` (kMaxDevices of them), or nullptr.
+inline DeviceOnce* device_slot(DeviceOnce* slots) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    return &slots[dev];
+}
 
 inline neo_status launch_status() {
     cudaError_t e = cudaGetLastError();

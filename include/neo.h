@@ -95,8 +95,11 @@ neo_status neo_build_positions(int32_t* indexes, int64_t S,
  * q: [S, Hq, D] and k: [S, Hkv, D] of `dtype` (bf16 or fp32), overwritten
  * with the result; arithmetic in fp32, one rounding to `dtype` at the end.
  * Either tensor may be NULL with its head count 0 (e.g. keys only).
- * indexes: int32 [3, S]. Norm weights: fp32 [64] each; the q weights may be
- * NULL when Hq == 0 and the k weights when Hkv == 0. D must be 128.
+ * indexes: int32 [3, S]; any int32 position is valid: each angle is reduced
+ * modulo 2 pi exactly (the frequency is held as a 64-bit fraction of a turn),
+ * so the angle error does not grow with the position. Norm weights: fp32 [64]
+ * each; the q weights may be NULL when Hq == 0 and the k weights when
+ * Hkv == 0. D must be 128. q and k must not overlap.
  * ------------------------------------------------------------------------ */
 neo_status neo_qknorm_rope3(void* q, void* k, neo_dtype dtype,
                             int64_t S, int Hq, int Hkv, int D,
@@ -236,6 +239,8 @@ neo_status neo_write_prefix_cache(const void* k_old, const void* v_old,
  *
  * z: fp32 [n], updated in place; x0_hat: fp32 [n]; v_out: optional fp32 [n]
  * receiving v, or NULL. fp32 arithmetic with a correctly rounded division.
+ * x0_hat and v_out must not overlap z or each other (the kernel reads and
+ * writes them without re-reading): an overlap returns NEO_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------ */
 neo_status neo_flow_euler_step(float* z, const float* x0_hat, int64_t n,
                                float t, float t_next, float t_eps,
@@ -257,7 +262,9 @@ neo_status neo_flow_euler_step(float* z, const float* x0_hat, int64_t n,
  *
  * z: fp32 [n] in place; x0_*: fp32 [n]; v_out: optional fp32 [n];
  * branch_out: optional HOST int32 receiving the branch taken.
- * Returns NEO_ERR_INVALID_ARG if a prediction the branch needs is NULL.
+ * Returns NEO_ERR_INVALID_ARG if a prediction the branch needs is NULL, or if
+ * v_out overlaps z or a prediction the branch reads, or a prediction overlaps
+ * z (predictions may share one buffer: they are only read).
  * ------------------------------------------------------------------------ */
 #define NEO_CFG_NONE 0
 #define NEO_CFG_TEXT 1
@@ -327,15 +334,19 @@ neo_status neo_rope2d_interleaved(void* x, neo_dtype dtype, int64_t n_images,
 /* Human-readable name of a status code (static string). */
 const char* neo_status_string(neo_status s);
 
-/* Synchronises `stream`, then returns the device error word accumulated by
- * earlier launches in *word (NEO_DEVERR_* bits) and clears it. Returns
+/* Synchronises `stream`, then returns the current device's error word
+ * accumulated by earlier launches on it in *word (NEO_DEVERR_* bits) and
+ * clears it (each device has its own word). Returns
  * NEO_ERR_TIMEOUT if the timeout bit was set, NEO_ERR_DEVICE for any other
  * bit, NEO_OK if the word was zero, NEO_ERR_CUDA on a CUDA failure.
  * `word` may be NULL. */
 neo_status neo_get_device_error(cudaStream_t stream, uint32_t* word);
 
 /* Sets the time limit of every pipeline wait inside the kernels, in
- * nanoseconds (default 1e9). Applies to launches enqueued afterwards. */
+ * nanoseconds (default 1e9), for the current device. Applies to launches
+ * enqueued afterwards. Kernel attributes and occupancy-derived launch sizes
+ * are set up once per device, the first time an entry point runs with that
+ * device current. */
 neo_status neo_set_wait_timeout_ns(uint64_t ns);
 
 /* Self-test of the kernels' bounded waits: one thread waits on a barrier

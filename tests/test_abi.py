@@ -48,6 +48,8 @@ def test_status_strings_and_version(lib):
 
 V = ctypes.c_void_p
 FAKE = V(0x10000)          # aligned, never dereferenced: the checks fail first
+FAKE2 = V(0x4000000)       # a second buffer that overlaps no other fake one at the sizes used here
+FAKE3 = V(0x8000000)
 MISALIGNED = V(0x10008)
 
 
@@ -88,7 +90,7 @@ def test_attention_rejects_bad_arguments(lib, kw, status):
 
 def test_qknorm_rope3_rejects_bad_arguments(lib):
     f = lib.neo_qknorm_rope3
-    args = [FAKE, FAKE, neo.NEO_BF16, 16, 4, 1, 128, FAKE, FAKE, FAKE, FAKE, FAKE, 5e6, 1e4, 1e-6, None]
+    args = [FAKE, FAKE2, neo.NEO_BF16, 16, 4, 1, 128, FAKE, FAKE, FAKE, FAKE, FAKE, 5e6, 1e4, 1e-6, None]
     bad = {6: 64, 2: 9, 0: MISALIGNED, 8: None, 12: -1.0, 14: float("inf"), 3: -5}
     for pos, val in bad.items():
         a = list(args)
@@ -100,15 +102,37 @@ def test_qknorm_rope3_rejects_bad_arguments(lib):
     a = list(args)
     a[7] = None                     # indexes missing
     assert f(*a) == neo.NEO_ERR_INVALID_ARG
+    a = list(args)
+    a[1] = V(0x10000 + 16 * 4 * 128 * 2 - 256)   # k starts inside q
+    assert f(*a) == neo.NEO_ERR_INVALID_ARG
 
 
 def test_euler_rejects_bad_arguments(lib):
     f = lib.neo_flow_euler_step
-    assert f(FAKE, FAKE, 0, 0.5, 0.6, 0.02, None, None) == neo.NEO_OK
-    assert f(None, FAKE, 8, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
-    assert f(MISALIGNED, FAKE, 8, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, 8, 1.0, 1.1, 0.0, None, None) == neo.NEO_ERR_INVALID_ARG   # max(1-t, t_eps) = 0
-    assert f(FAKE, FAKE, 8, float("nan"), 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(FAKE, FAKE2, 0, 0.5, 0.6, 0.02, None, None) == neo.NEO_OK
+    assert f(None, FAKE2, 8, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(MISALIGNED, FAKE2, 8, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(FAKE, FAKE2, 8, 1.0, 1.1, 0.0, None, None) == neo.NEO_ERR_INVALID_ARG   # max(1-t, t_eps) = 0
+    assert f(FAKE, FAKE2, 8, float("nan"), 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+
+
+def test_euler_rejects_overlapping_buffers(lib):
+    """z is read and written, x0_hat read, v_out written: any overlap between
+    them would let one element's write change another's input."""
+    f = lib.neo_flow_euler_step
+    n = 1024
+    assert f(FAKE, FAKE, n, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG            # x0_hat is z
+    assert f(FAKE, V(0x10000 + 4 * n - 16), n, 0.5, 0.6, 0.02, None, None) == neo.NEO_ERR_INVALID_ARG
+    assert f(FAKE, FAKE2, n, 0.5, 0.6, 0.02, FAKE, None) == neo.NEO_ERR_INVALID_ARG          # v_out is z
+    assert f(FAKE, FAKE2, n, 0.5, 0.6, 0.02, FAKE2, None) == neo.NEO_ERR_INVALID_ARG         # v_out is x0_hat
+    fc = lib.neo_flow_cfg_euler_step
+    # dual CFG: z overlapping a prediction, v_out overlapping z or a prediction
+    assert fc(FAKE, FAKE, FAKE2, FAKE3, n, 0.5, 0.6, 0.02, 4.0, 1.5, 0.0, 1.0, None, None, None) == \
+        neo.NEO_ERR_INVALID_ARG
+    assert fc(FAKE, FAKE2, FAKE3, V(0xC000000), n, 0.5, 0.6, 0.02, 4.0, 1.5, 0.0, 1.0, FAKE3, None, None) == \
+        neo.NEO_ERR_INVALID_ARG
+    assert fc(FAKE, FAKE2, FAKE3, V(0xC000000), n, 0.5, 0.6, 0.02, 4.0, 1.5, 0.0, 1.0, FAKE, None, None) == \
+        neo.NEO_ERR_INVALID_ARG
 
 
 def test_positions_rejects_bad_segments(lib):

@@ -908,6 +908,8 @@ struct Unit {
     int b, kvh, n0, lo, L, n_pre, n_tiles;
     bool ok;                                       // consistent prefix offsets
     int j_diag, tmin, tmax;                        // kBC: the diagonal image tile; the queries' T range
+    int run;                                       // kBC: key tiles [0, run) are the prefix tiles and image
+                                                   // tiles 0, 1, ..., every key visible to every row of this CTA
 };
 
 // kBC: the image tile after t (-1: the first) in a unit's key sequence.
@@ -968,6 +970,7 @@ __device__ __forceinline__ Unit finish_unit(const AttnParams& p, const UnitLoad&
     u.j_diag = n_img - 1;
     u.tmin = INT_MIN;
     u.tmax = INT_MAX;
+    u.run = u.n_tiles;
     if constexpr (kBC) {
         // The cluster's queries are image tokens [np0, np1): their T range from
         // the 64-key halves holding them (a superset for pairs of under 64 tokens).
@@ -995,11 +998,14 @@ __device__ __forceinline__ Unit finish_unit(const AttnParams& p, const UnitLoad&
                 cnt += __popc(__ballot_sync(0xffffffffu, kept));
             }
             u.n_tiles = u.ok ? u.n_pre + cnt : 0;
+            u.run = 0;
         } else {
-            // Counted once in the prologue (unit k of this cluster: U = cluster + k * clusters).
+            // Counted once in the prologue (unit k of this cluster: U = cluster + k * clusters):
+            // the image tiles of the key sequence (low 16 bits) and of the run (high 16 bits).
             const int ncl = (int)(gridDim.x / kCluster), cid = (int)(blockIdx.x / kCluster);
-            const int cnt = reinterpret_cast<const int*>(smem + kSmUnitTiles)[(l.U - cid) / ncl];
-            u.n_tiles = u.ok ? u.n_pre + cnt : 0;
+            const int packed = reinterpret_cast<const int*>(smem + kSmUnitTiles)[(l.U - cid) / ncl];
+            u.n_tiles = u.ok ? u.n_pre + (packed & 0xffff) : 0;
+            u.run = u.ok ? u.n_pre + (packed >> 16) : 0;
         }
     }
     return u;
@@ -1008,6 +1014,51 @@ __device__ __forceinline__ Unit finish_unit(const AttnParams& p, const UnitLoad&
 template <bool kBC, bool kWarp = false>
 __device__ __forceinline__ Unit decode(const AttnParams& p, int U, int pairs, uint32_t crank, const uint8_t* smem) {
     return finish_unit<kBC, kWarp>(p, load_unit(p, U, pairs), pairs, crank, smem);
+}
+
+// kBC, all 32 lanes: the number of image tiles at the head of unit u's key
+// sequence (tiles 0, 1, ... with none skipped) whose every key is visible to
+// every row of this CTA, so that the softmax takes them without the per-row
+// classification. Query rows are image tokens [n0, n1] (i = L + n); key k of
+// an image tile (j = L + k) is visible to all of them if k <= n0 (at or
+// before every query), and a 64-key half is visible as a whole if its last
+// existing key is, or if its keys and the queries share one temporal index.
+// Prefix keys precede every query and are always visible. A CTA whose rows
+// are all padding (n0 >= N) stores nothing: its run is the kept prefix.
+__device__ __forceinline__ int bc_visible_run(const AttnParams& p, const Unit& u, const int4* tile_t, int n_img) {
+    const int lane = (int)(threadIdx.x & 31);
+    // The queries' temporal range, from the ranges of the 64-key halves that
+    // hold them (a superset: at worst the run ends earlier than it could).
+    const int n1 = min(p.N, u.n0 + p.tok_per_tile) - 1;
+    int qlo = INT_MAX, qhi = INT_MIN;
+    for (int h = u.n0 / 64; h <= n1 / 64; ++h) {
+        const int4 r = tile_t[h >> 1];
+        qlo = min(qlo, (h & 1) ? r.z : r.x);
+        qhi = max(qhi, (h & 1) ? r.w : r.y);
+    }
+    const bool one_t = qlo == qhi;
+    for (int t0 = 0; t0 < n_img; t0 += 32) {
+        const int t = t0 + lane;
+        bool good = false;
+        if (t < n_img) {
+            const int4 r = tile_t[t];
+            const bool kept = t <= u.j_diag || (r.x <= u.tmax && r.y >= u.tmin) || (r.z <= u.tmax && r.w >= u.tmin);
+            bool full = true;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int lo = h ? r.z : r.x, hi = h ? r.w : r.y;
+                const int last = min(p.N - 1, t * kBlockN + 64 * h + 63);
+                const bool empty = lo > hi;
+                const bool before = last <= u.n0;
+                const bool shared = one_t && lo == qlo && hi == qlo;
+                full = full && (empty || before || shared || u.n0 >= p.N);
+            }
+            good = kept && full;
+        }
+        const uint32_t bad = __ballot_sync(0xffffffffu, !good);
+        if (bad) return t0 + __ffs(bad) - 1;
+    }
+    return n_img;
 }
 
 }  // namespace pk
@@ -1117,9 +1168,11 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         __syncthreads();
         // The image key tiles of each of this cluster's units, one warp a unit.
         int* unit_tiles = reinterpret_cast<int*>(smem + pk::kSmUnitTiles);
+        const uint32_t rank = cluster_ctarank();
         for (int k = warp; cid + k * ncl < n_units; k += kThreads / 32) {
-            const Unit u = pk::decode<true, true>(p, cid + k * ncl, pairs, 0, smem);
-            if (lane == 0) unit_tiles[k] = u.n_tiles - u.n_pre;
+            const Unit u = pk::decode<true, true>(p, cid + k * ncl, pairs, rank, smem);
+            const int run = u.ok ? pk::bc_visible_run(p, u, tile_t, n_img) : 0;
+            if (lane == 0) unit_tiles[k] = (u.n_tiles - u.n_pre) | (run << 16);
         }
     }
     tc_fence_before();
@@ -1418,7 +1471,8 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 // row pair still meet at every pair barrier.
                 for (int j = 0; j < u.n_tiles; ++j, ++gt) {
                     if (j >= u.n_pre)
-                        it = kBC ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
+                        it = kBC && j >= u.run
+                                 ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
                                  : j - u.n_pre;
                     const int sbuf = gt % kSBufs;
                     const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
@@ -1429,7 +1483,11 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
                     bool partial = valid < 64;
                     uint64_t keep = 0;                           // kBC: bit c = key column c is visible
-                    if constexpr (kBC) {
+                    bool masked = partial;                       // warp-uniform (see below)
+                    if (kBC && j < u.run) {
+                        // Every key of the tile is visible to every row: the segment end only.
+                        keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
+                    } else if constexpr (kBC) {
                         // Key j of [prefix ; image] is visible to query i iff T_j == T_i or
                         // j <= i ("Block-causal attention"). This row's 64 keys: all at or
                         // before the row or all sharing its index -> the segment-end mask
@@ -1453,10 +1511,11 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                             }
                         }
                         partial = keep != ~0ull;
+                        // Warp-uniform, so that the per-element mask below is a branch that
+                        // full tiles skip (with the full mask, and within the run, the tile
+                        // alone decides it).
+                        masked = __any_sync(0xffffffffu, partial);
                     }
-                    // Warp-uniform, so that the per-element mask below is a branch that
-                    // full tiles skip (with the full mask it depends on the tile only).
-                    const bool masked = kBC ? __any_sync(0xffffffffu, partial) : partial;
                     float* mx_tile = mx_s + (gt & 1) * 256;
                     if (ok) {
                         tc_fence_after();

@@ -241,12 +241,15 @@ def test_many_short_units_per_cluster(gpu_lib):
     assert torch.isfinite(out).all()
 
 
-@pytest.mark.parametrize("case", ["mixed", "chunked", "unordered", "random", "g1"])
+@pytest.mark.parametrize("case", ["mixed", "chunked", "unordered", "random", "g1", "rounds"])
 def test_block_causal_one_sequence_equals_batched(gpu_lib, case):
     """One sequence runs in the persistent kernel, a batch of two in the
     one-tile-per-CTA kernel; each sequence of the batch, run alone, gives the
     same bits (tiles the persistent kernel keeps beyond the exact set are fully
-    masked and add exact zeros)."""
+    masked and add exact zeros). "rounds": 3000 tokens, 94 units for at most
+    76 clusters, so the persistent kernel's clusters take a second, partial
+    round; the runs of fully visible tiles at the head of each unit's key
+    sequence start with prefix, text and image keys."""
     rng = np.random.default_rng(21)
     Hq, Hkv = 8, 2
     if case == "mixed":
@@ -260,6 +263,9 @@ def test_block_causal_one_sequence_equals_batched(gpu_lib, case):
     elif case == "random":
         pre = [rng.integers(0, 40, size=50).tolist(), rng.integers(0, 400, size=90).tolist()]
         img = [rng.integers(0, 40, size=333).tolist(), rng.integers(0, 400, size=333).tolist()]
+    elif case == "rounds":
+        a, b = _mixed_T(500, 2300, 260), _mixed_T(90, 2600, 370)
+        pre, img = [a[:60], b[:60]], [a[60:], b[60:]]
     else:
         pre, img, Hq, Hkv = [[], []], [_mixed_T(100, 256, 20), _mixed_T(20, 256, 100)], 2, 2
     B, N = 2, len(img[0])

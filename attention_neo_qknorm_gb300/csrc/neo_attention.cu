@@ -1254,7 +1254,8 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     int it = -1;                   // image tile of key tile j
                     for (int j = 0; ok && j < u.n_tiles; ++j) {
                         if (j >= u.n_pre)
-                            it = kBC ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
+                            it = kBC && j >= u.run
+                                     ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
                                      : j - u.n_pre;
                         const int st = gt % stages;
                         if (!wait(bar(sb, empty0 + st), ((uint32_t)(gt / stages) & 1u) ^ 1u)) {
@@ -1481,41 +1482,12 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     float pmax = -INFINITY;
                     const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
                     const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
-                    bool partial = valid < 64;
-                    uint64_t keep = 0;                           // kBC: bit c = key column c is visible
-                    bool masked = partial;                       // warp-uniform (see below)
-                    if (kBC && j < u.run) {
-                        // Every key of the tile is visible to every row: the segment end only.
-                        keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
-                    } else if constexpr (kBC) {
-                        // Key j of [prefix ; image] is visible to query i iff T_j == T_i or
-                        // j <= i ("Block-causal attention"). This row's 64 keys: all at or
-                        // before the row or all sharing its index -> the segment-end mask
-                        // only; the row's index outside the keys' range -> causal, a
-                        // threshold; otherwise (a block boundary) key by key.
-                        const int key0 = (j < u.n_pre ? j * kBlockN : u.L + it * kBlockN) + half * 64;
-                        keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
-                        if (j >= u.n_pre && key0 + 63 > i_row) {
-                            const int4 tr = reinterpret_cast<const int4*>(smem + pk::kSmTileTP)[it];
-                            const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
-                            if (!(klo == t_row && khi == t_row)) {
-                                const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
-                                const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
-                                if (t_row < klo || t_row > khi) {
-                                    keep &= causal;
-                                } else {
-                                    const int32_t* tk = p.t_img + (key0 - u.L);
-                                    for (int c = max(lim, 0); c < min(valid, 64); ++c)
-                                        if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
-                                }
-                            }
-                        }
-                        partial = keep != ~0ull;
-                        // Warp-uniform, so that the per-element mask below is a branch that
-                        // full tiles skip (with the full mask, and within the run, the tile
-                        // alone decides it).
-                        masked = __any_sync(0xffffffffu, partial);
-                    }
+                    // Keys past the end of the prefix or image segment do not exist. With
+                    // the full mask, and on the block-causal tiles of a unit's run, that is
+                    // the only mask, and warp-uniform: the per-element mask below is then a
+                    // branch that full tiles skip.
+                    const bool partial = valid < 64;
+                    const bool classify = kBC && j >= u.run;     // warp-uniform
                     float* mx_tile = mx_s + (gt & 1) * 256;
                     if (ok) {
                         tc_fence_after();
@@ -1525,17 +1497,43 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     #pragma unroll
                             for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
                         }
-                        // Keys past the end of the prefix or image segment do not exist.
-                        if (masked) {
-                            // An opaque statement keeps this block behind its branch: the
-                            // compiler would otherwise turn it into selects run on every tile.
-                            asm volatile("");
+                        if (!classify) {
+                            if (partial) {
+                                // An opaque statement keeps this block behind its branch: the
+                                // compiler would otherwise turn it into selects run on every tile.
+                                asm volatile("");
     #pragma unroll
-                            for (int c = 0; c < 64; ++c) {
-                                bool vis;
-                                if constexpr (kBC) vis = (keep >> c) & 1u;
-                                else vis = c < valid;
-                                s[c] = vis ? s[c] : -INFINITY;
+                                for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                            }
+                        } else if constexpr (kBC) {
+                            // A tile outside the unit's run, classified per row once S is in
+                            // registers (so that none of this state is live across the load).
+                            // Key j of [prefix ; image] is visible to query i iff T_j == T_i or
+                            // j <= i ("Block-causal attention"). This row's 64 keys: all at or
+                            // before the row or all sharing its index -> the segment-end mask
+                            // only; the row's index outside the keys' range -> causal, a
+                            // threshold; otherwise (a block boundary) key by key.
+                            const int key0 = (j < u.n_pre ? j * kBlockN : u.L + it * kBlockN) + half * 64;
+                            uint64_t keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
+                            if (j >= u.n_pre && key0 + 63 > i_row) {
+                                const int4 tr = reinterpret_cast<const int4*>(smem + pk::kSmTileTP)[it];
+                                const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
+                                if (!(klo == t_row && khi == t_row)) {
+                                    const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
+                                    const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
+                                    if (t_row < klo || t_row > khi) {
+                                        keep &= causal;
+                                    } else {
+                                        const int32_t* tk = p.t_img + (key0 - u.L);
+                                        for (int c = max(lim, 0); c < min(valid, 64); ++c)
+                                            if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
+                                    }
+                                }
+                            }
+                            if (__any_sync(0xffffffffu, keep != ~0ull)) {
+                                asm volatile("");
+    #pragma unroll
+                                for (int c = 0; c < 64; ++c) s[c] = ((keep >> c) & 1u) ? s[c] : -INFINITY;
                             }
                         }
                         // Partial row maximum of the raw logits (three-input max tree).

@@ -1168,9 +1168,11 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         __syncthreads();
         // The image key tiles of each of this cluster's units, one warp a unit.
         int* unit_tiles = reinterpret_cast<int*>(smem + pk::kSmUnitTiles);
+        // One sequence (the only case this kernel takes the block-causal mask
+        // for): every unit's prefix offsets are the first unit's, already loaded.
         const uint32_t rank = cluster_ctarank();
         for (int k = warp; cid + k * ncl < n_units; k += kThreads / 32) {
-            const Unit u = pk::decode<true, true>(p, cid + k * ncl, pairs, rank, smem);
+            const Unit u = pk::finish_unit<true, true>(p, UnitLoad{cid + k * ncl, first.lo, first.hi}, pairs, rank, smem);
             const int run = u.ok ? pk::bc_visible_run(p, u, tile_t, n_img) : 0;
             if (lane == 0) unit_tiles[k] = (u.n_tiles - u.n_pre) | (run << 16);
         }

@@ -227,6 +227,8 @@ def test_scale_noise_and_sampler_loop(gpu_lib):
     (torch.bfloat16, 1, 3, 4, 4096),      # more 16-byte chunks per patch than threads per block
     (torch.bfloat16, 700, 3, 3, 8),       # one chunk per patch: many patches per block
     (torch.float32, 2, 7, 3, 12),         # fp32 chunks straddle the halves
+    (torch.bfloat16, 2, 17, 9, 32),       # lines longer than one segment, ragged last segments
+    (torch.float32, 1, 1, 19, 16),        # one row: every column line a single patch
 ])
 def test_rope2d_interleaved_matches_oracle(gpu_lib, dtype, n_img, rows, cols, C):
     gen = torch.Generator().manual_seed(rows * cols + C)

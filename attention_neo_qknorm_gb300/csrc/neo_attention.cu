@@ -1061,6 +1061,58 @@ __device__ __forceinline__ int bc_visible_run(const AttnParams& p, const Unit& u
     return n_img;
 }
 
+// kBC, off the tile loop's hot path: the next kept image tile after t past
+// the unit's diagonal (bc_next out of line, so that its walk takes no
+// registers in the loop of the common case).
+__device__ __noinline__ int bc_next_cold(const int4* tile_t, Unit u, int t, int n_img) {
+    return bc_next(tile_t, u, t, n_img);
+}
+
+// kBC, off the tile loop's hot path: the per-row mask of one 64-key half of
+// key tile j outside the unit's run, written into S in TMEM (hidden keys
+// become -inf) before the softmax loads it; called by a whole warp. Key j of
+// [prefix ; image] is visible to query i iff T_j == T_i or j <= i
+// ("Block-causal attention"). This row's 64 keys: all at or before the row or
+// all sharing its index -> nothing to hide beyond the segment end, which the
+// softmax masks itself; the row's index outside the keys' range -> causal, a
+// threshold; otherwise (a block boundary) key by key. The row is image token
+// n_row of the sequence (i = L + n_row).
+__device__ __noinline__ void bc_mask_s_cold(uint32_t taddr, const int32_t* t_img, const int4* tile_t, int j, int n_pre,
+                                            int L, int it, int half, int valid, int n_row) {
+    const int i_row = L + n_row;
+    const int t_row = __ldg(t_img + n_row);
+    const int key0 = (j < n_pre ? j * kBlockN : L + it * kBlockN) + half * 64;
+    uint64_t keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
+    if (j >= n_pre && key0 + 63 > i_row) {
+        const int4 tr = tile_t[it];
+        const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
+        if (!(klo == t_row && khi == t_row)) {
+            const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
+            const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
+            if (t_row < klo || t_row > khi) {
+                keep &= causal;
+            } else {
+                const int32_t* tk = t_img + (key0 - L);
+                for (int c = max(lim, 0); c < min(valid, 64); ++c)
+                    if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
+            }
+        }
+    }
+    if (!__any_sync(0xffffffffu, keep != ~0ull)) return;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        tmem_ld32(taddr + 32u * (uint32_t)h, r);
+        const uint32_t kw = (uint32_t)(keep >> (32 * h));
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (!((kw >> c) & 1u)) r[c] = __float_as_uint(-INFINITY);
+        tmem_st32(taddr + 32u * (uint32_t)h, r);
+    }
+    tmem_st_wait();
+}
+
 }  // namespace pk
 
 template <bool kBC, bool kQN>
@@ -1463,19 +1515,19 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             float l_part = 0.f;
             if (u.n_tiles > 0) {
                 // kBC: this row's query is image token n_row (clamped for padding
-                // rows, whose output is never stored), i_row = L + n_row in the
-                // concatenated order [prefix ; image], with temporal index t_row.
+                // rows, whose output is never stored), L + n_row in the
+                // concatenated order [prefix ; image].
                 const int n_row = min(u.n0 + row / p.G, p.N - 1);
-                const int i_row = u.L + n_row;
-                const int t_row = kBC ? __ldg(p.t_img + n_row) : 0;
                 int it = -1;                       // image tile of key tile j
                 // A failed wait sets `failed`: the loops then keep running without
                 // touching TMEM or the pipeline barriers, so that the two warps of a
                 // row pair still meet at every pair barrier.
                 for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                    // Image tiles up to the diagonal and those of the run follow one
+                    // another; only kept tiles past both are looked up.
                     if (j >= u.n_pre)
-                        it = kBC && j >= u.run
-                                 ? pk::bc_next(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
+                        it = kBC && j >= u.run && j - u.n_pre > u.j_diag
+                                 ? pk::bc_next_cold(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
                                  : j - u.n_pre;
                     const int sbuf = gt % kSBufs;
                     const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
@@ -1484,59 +1536,30 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                     float pmax = -INFINITY;
                     const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
                     const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
-                    // Keys past the end of the prefix or image segment do not exist. With
-                    // the full mask, and on the block-causal tiles of a unit's run, that is
-                    // the only mask, and warp-uniform: the per-element mask below is then a
-                    // branch that full tiles skip.
+                    // Keys past the end of the prefix or image segment do not exist:
+                    // warp-uniform, so the per-element mask below is a branch that
+                    // full tiles skip. A block-causal tile outside the unit's run also
+                    // has its hidden keys written into S first (out of line).
                     const bool partial = valid < 64;
-                    const bool classify = kBC && j >= u.run;     // warp-uniform
                     float* mx_tile = mx_s + (gt & 1) * 256;
                     if (ok) {
                         tc_fence_after();
+                        if (kBC && j >= u.run)   // warp-uniform
+                            pk::bc_mask_s_cold(lane_base + scol + (uint32_t)half * 64u, p.t_img,
+                                               reinterpret_cast<const int4*>(smem + pk::kSmTileTP), j, u.n_pre, u.L,
+                                               it, half, valid, n_row);
                         {
                             uint32_t r[64];
                             tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
     #pragma unroll
                             for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
                         }
-                        if (!classify) {
-                            if (partial) {
-                                // An opaque statement keeps this block behind its branch: the
-                                // compiler would otherwise turn it into selects run on every tile.
-                                asm volatile("");
+                        if (partial) {
+                            // An opaque statement keeps this block behind its branch: the
+                            // compiler would otherwise turn it into selects run on every tile.
+                            asm volatile("");
     #pragma unroll
-                                for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
-                            }
-                        } else if constexpr (kBC) {
-                            // A tile outside the unit's run, classified per row once S is in
-                            // registers (so that none of this state is live across the load).
-                            // Key j of [prefix ; image] is visible to query i iff T_j == T_i or
-                            // j <= i ("Block-causal attention"). This row's 64 keys: all at or
-                            // before the row or all sharing its index -> the segment-end mask
-                            // only; the row's index outside the keys' range -> causal, a
-                            // threshold; otherwise (a block boundary) key by key.
-                            const int key0 = (j < u.n_pre ? j * kBlockN : u.L + it * kBlockN) + half * 64;
-                            uint64_t keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
-                            if (j >= u.n_pre && key0 + 63 > i_row) {
-                                const int4 tr = reinterpret_cast<const int4*>(smem + pk::kSmTileTP)[it];
-                                const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
-                                if (!(klo == t_row && khi == t_row)) {
-                                    const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
-                                    const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
-                                    if (t_row < klo || t_row > khi) {
-                                        keep &= causal;
-                                    } else {
-                                        const int32_t* tk = p.t_img + (key0 - u.L);
-                                        for (int c = max(lim, 0); c < min(valid, 64); ++c)
-                                            if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
-                                    }
-                                }
-                            }
-                            if (__any_sync(0xffffffffu, keep != ~0ull)) {
-                                asm volatile("");
-    #pragma unroll
-                                for (int c = 0; c < 64; ++c) s[c] = ((keep >> c) & 1u) ? s[c] : -INFINITY;
-                            }
+                            for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
                         }
                         // Partial row maximum of the raw logits (three-input max tree).
                         float t1[22];

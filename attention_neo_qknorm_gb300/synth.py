@@ -167,14 +167,3 @@ def make_flow(w: Workload, seed: int | None = None, n_x0: int = 1):
     z = torch.randn(w.B * w.N, PATCH_ELEMS, generator=g, dtype=torch.float32)
     x0 = [torch.randn(w.B * w.N, PATCH_ELEMS, generator=g, dtype=torch.float32) for _ in range(n_x0)]
     return z, x0
-
-
-def random_rows(w: Workload, count: int, seed: int = 0) -> np.ndarray:
-    """``count`` distinct (b, n, h) query rows, seeded, for sampled checks."""
-    rng = np.random.default_rng(seed)
-    total = w.B * w.N * w.Hq
-    flat = rng.choice(total, size=min(count, total), replace=False)
-    b = flat // (w.N * w.Hq)
-    n = (flat // w.Hq) % w.N
-    h = flat % w.Hq
-    return np.stack([b, n, h], axis=1).astype(np.int64)

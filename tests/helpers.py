@@ -59,8 +59,3 @@ def oracle_layer(w, inp, rows=None):
     q, k = oracle_norm_rope(w, inp)
     kp = oracle_prefix_keys(w, inp)
     return O.gen_attention(q, kp, f64(inp.v_prefix), k, f64(inp.v), w.cu_prefix, SCALE, rows=rows)
-
-
-def take_rows(t: np.ndarray, rows):
-    """out [B, N, Hq, D] -> [R, D] for (b, n, h) rows."""
-    return np.stack([t[b, n, h] for b, n, h in rows])

@@ -36,17 +36,22 @@
 //     shared memory, O accumulated in TMEM). Issuing a batch blocks while the
 //     tensor pipe's queue is full, so two independent issuers keep it fed
 //     while either one waits on a barrier.
-//   * Warps 4..11 run the online softmax in fp32. Query row r is TMEM lane r;
-//     warps 4..7 own its key columns [0,64) and warps 8..11 columns [64,128)
-//     (the same TMEM lanes, two warps per sub-partition). The two halves of a
-//     row exchange only their partial maximum through shared memory; each
-//     keeps its own partial row sum until the end. exp2 runs on the SFU; P_j
-//     goes to TMEM as bf16 over the first 64 columns of the S buffer it came
-//     from, so S_j reuses a buffer only once PV_{j-3} has read it and the
-//     softmax never waits for PV. O is rescaled only when the running maximum
-//     grew by more than 2^8 (the final division uses the same stale maximum,
-//     so the result is unchanged). Each half finally writes its 64-wide half
-//     of O / l as bf16 through shared memory and a TMA store.
+//   * Warps 4..11 run the online softmax in fp32. Query row r is TMEM lane r.
+//     Warps w and w + 4 share the lanes of sub-partition w & 3 and each owns
+//     16 whole rows of it, loaded with the 16-lane tcgen05.ld shape: a thread
+//     holds two rows (r, r + 8) and 32 of their 128 key columns, so a row's
+//     maximum is reduced over four threads of one warp with two shuffles and
+//     the two warps of a sub-partition never wait for each other within a
+//     unit. Each thread keeps partial row sums until the end. exp2 runs on
+//     the SFU; P_j goes to TMEM as bf16 (16x128b stores, whose layout is the
+//     packed form of the 16x256b load's) over the rows' own first 64 columns
+//     of the S buffer it came from, so S_j reuses a buffer only once PV_{j-3}
+//     has read it and the softmax never waits for PV. O is rescaled only when
+//     the running maximum grew by more than 2^8 (the final division uses the
+//     same stale maximum, so the result is unchanged). The epilogue reads O
+//     one row a thread, each warp a 64-wide half of the columns of all 32
+//     rows (sums and maxima through shared memory), and writes O / l as bf16
+//     through shared memory and a TMA store.
 // TMEM: S0 [0,128) S1 [128,256) S2 [256,384) O [384,512).
 
 #include <algorithm>
@@ -300,6 +305,77 @@ __device__ __forceinline__ void qnorm_rope_q_half_lowreg(uint8_t* half_tile, int
         *reinterpret_cast<uint4*>(rowp + ((pa[s] ^ (row & 7)) << 4)) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
         *reinterpret_cast<uint4*>(rowp + ((pb[s] ^ (row & 7)) << 4)) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
     }
+}
+
+// max of 32 values: three-input max tree (11, 4, 1).
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float t[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) t[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    t[10] = fmaxf(v[30], v[31]);
+    const float u0 = fmax3(t[0], t[1], t[2]), u1 = fmax3(t[3], t[4], t[5]), u2 = fmax3(t[6], t[7], t[8]);
+    return fmaxf(fmax3(u0, u1, u2), fmaxf(t[9], t[10]));
+}
+
+// Block-causal mode: the keep bits of one 64-key half of key tile j for one query row
+// (bit c: key key0 + c). Key j of [prefix ; image] is visible to query i iff
+// T_j == T_i or j <= i ("Block-causal attention"). The row's 64 keys all at or
+// before the row or all sharing its index -> nothing to hide beyond the
+// segment end; the row's index outside the keys' range -> causal, a
+// threshold; otherwise (a block boundary) key by key. i_row = L + the row's
+// image token, t_row its temporal index; t_img: the sequence's image tokens.
+__device__ __forceinline__ uint64_t bc_keep_half(const int32_t* t_img, const int4* tile_t, int j, int n_pre, int L,
+                                                 int it, int half, int valid, int i_row, int t_row) {
+    const int key0 = (j < n_pre ? j * kBlockN : L + it * kBlockN) + half * 64;
+    uint64_t keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
+    if (j >= n_pre && key0 + 63 > i_row) {
+        const int4 tr = tile_t[it];
+        const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
+        if (!(klo == t_row && khi == t_row)) {
+            const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
+            const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
+            if (t_row < klo || t_row > khi) {
+                keep &= causal;
+            } else {
+                const int32_t* tk = t_img + (key0 - L);
+                for (int c = max(lim, 0); c < min(valid, 64); ++c)
+                    if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
+            }
+        }
+    }
+    return keep;
+}
+
+// Block-causal mode, off the tile loop's hot path, for the 16-lane softmax
+// layout: the mask of key tile j for this thread's two rows
+// (image tokens n_a, n_b), written into S in TMEM (hidden keys become -inf)
+// before the softmax loads it; called by a whole warp. taddr: the S buffer
+// at the warp's 16 lanes; jq: the thread's column group.
+__device__ __noinline__ void bc_mask_s_cold16(uint32_t taddr, const int32_t* t_img, const int4* tile_t, int j,
+                                              int n_pre, int L, int it, int tile_valid, int n_a, int n_b, int jq) {
+    uint64_t keep[2][2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int n_row = r ? n_b : n_a;
+        const int t_row = __ldg(t_img + n_row);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            keep[r][h] = bc_keep_half(t_img, tile_t, j, n_pre, L, it, h, tile_valid - 64 * h, L + n_row, t_row);
+    }
+    if (!__any_sync(0xffffffffu, (keep[0][0] & keep[0][1] & keep[1][0] & keep[1][1]) != ~0ull)) return;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        tmem_ld16x256b_x8(taddr + 64u * (uint32_t)h, r);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (!((keep[e >> 1][h] >> (8 * k + 2 * jq + (e & 1))) & 1ull)) r[4 * k + e] = __float_as_uint(-INFINITY);
+        tmem_st16x256b_x8(taddr + 64u * (uint32_t)h, r);
+    }
+    tmem_st_wait();
 }
 
 // kQNorm: the query norm + RoPE is folded into the prologue (a separate
@@ -567,15 +643,25 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax + epilogue
-        const int half = (warp - 4) >> 2;          // key columns [64*half, 64*half + 64)
+        // Warps w and w + 4 share the TMEM lanes of quadrant w & 3 and each owns
+        // 16 of its rows, read and written with the 16-lane shapes: thread
+        // 4i + jq holds rows i and i + 8 of the 16, key columns 8k + 2jq and
+        // 8k + 2jq + 1 of every group of eight. A row's maximum and sum stay
+        // within one warp (four threads), so the two warps do not meet per tile.
+        const int hw = (warp - 4) >> 2;
         const int quad = warp & 3;
+        const int jq = lane & 3;
+        const int row_a = quad * 32 + hw * 16 + (lane >> 2);   // and row_a + 8
+        const uint32_t lane16 = tmem + ((uint32_t)(quad * 32 + hw * 16) << 16);
+        // The epilogue reads O one row a thread (all 32 rows of the quadrant),
+        // 64 of its columns a warp.
+        const int half = hw;
         const int row = quad * 32 + lane;
-        const uint32_t pair_bar = 2u + (uint32_t)quad;   // the two warps sharing these TMEM lanes
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        float* mx_s = reinterpret_cast<float*>(smem + kSmMax);
-        float* ls_s = reinterpret_cast<float*>(smem + kSmLsum);
-        float m_used = -INFINITY;
-        float l_part = 0.f;
+        float* mx_s = reinterpret_cast<float*>(smem + kSmMax);    // the rows' maxima, [128]
+        float* ls_s = reinterpret_cast<float*>(smem + kSmLsum);   // the rows' sums, [128]
+        float m_a = -INFINITY, m_b = -INFINITY;   // running maxima of rows a and a + 8 (log2 units)
+        float l_a = 0.f, l_b = 0.f;               // this thread's part of their sums
         bool failed = false;
         if constexpr (kQNorm) {
             // Folded query norm + RoPE: thread t normalises and rotates one
@@ -608,143 +694,123 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 failed = true;
             }
         }
-        // Block-causal mode (section "Block-causal attention"): key j of the
-        // concatenated order [prefix ; image] is visible to query i iff
-        // T_j == T_i or j <= i. This row's query is image token n (clamped for
-        // padding rows, whose output is never stored), i = L + n.
-        constexpr bool block_causal = kBlockCausal;
-        const int n_row = min(n0 + row / p.G, p.N - 1);
-        const int i_row = L + n_row;
-        const int t_row = block_causal ? __ldg(p.t_img + (int64_t)b * p.N + n_row) : 0;
-        // A failed (timed-out or aborted) wait sets `failed`. The loop then keeps
-        // running without touching TMEM or the pipeline barriers, so that the
-        // two warps of a row pair still meet at every pair barrier.
+        // Block-causal mode: the rows' queries are image tokens n_a, n_b
+        // (clamped for padding rows, whose output is never stored).
+        const int n_a = min(n0 + row_a / p.G, p.N - 1);
+        const int n_b = min(n0 + (row_a + 8) / p.G, p.N - 1);
+        const int32_t* t_seq = kBlockCausal ? p.t_img + (int64_t)b * p.N : nullptr;
+        // A failed (timed-out or aborted) wait sets `failed`; the loop then runs
+        // on without touching TMEM or the pipeline barriers.
         for (int j = 0; j < n_tiles; ++j) {
+            if (failed) continue;
             const int sbuf = j % kSBufs;
             const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
-            bool ok = !failed && __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + sbuf), (uint32_t)(j / kSBufs) & 1u));
-            float s[64];
-            float pmax = -INFINITY;
+            if (!__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_S_FULL + sbuf), (uint32_t)(j / kSBufs) & 1u))) {
+                failed = true;
+                continue;
+            }
             const int it = j < n_pre ? 0 : img_tile(j - n_pre);   // image tile index
             const int tile_valid = j < n_pre ? min(kBlockN, L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
-            const int valid = tile_valid - half * 64;        // may be <= 0: this half is all padding
-            // Concatenated index of this thread's first key column.
-            const int key0 = (j < n_pre ? j * kBlockN : L + it * kBlockN) + half * 64;
-            bool partial = valid < 64;
-            uint64_t keep = 0;                               // bit c: key column c is visible
-            if constexpr (block_causal) {
-                // Classify this row's 64 keys: all at or before the row (i) or all
-                // sharing its temporal index -> the segment-end mask only; the
-                // row's index outside the keys' range -> causal, a threshold;
-                // otherwise (a block boundary) key by key.
-                keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
-                if (j >= n_pre && key0 + 63 > i_row) {
-                    const int4 tr = reinterpret_cast<const int4*>(smem + kSmTileT)[it];
-                    const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
-                    if (!(klo == t_row && khi == t_row)) {
-                        const int lim = i_row - key0 + 1;       // columns c < lim are at or before the row
-                        const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
-                        if (t_row < klo || t_row > khi) {
-                            keep &= causal;
-                        } else {
-                            const int32_t* tk = p.t_img + (int64_t)b * p.N + (key0 - L);
-                            for (int c = max(lim, 0); c < min(valid, 64); ++c)
-                                if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
-                        }
-                    }
-                }
-                partial = keep != ~0ull;
-            }
-            // Full mask: only keys past the segment's end are hidden (a plain
-            // compare, cheaper in the hot loops than testing a bit of `keep`).
-            auto visible = [&](int c) -> bool {
-                if constexpr (block_causal) return (keep >> c) & 1u;
-                else return c < valid;
-            };
-            // Warp-uniform, so that the per-element mask below is a branch that
-            // full tiles skip (with the full mask it depends on the tile only).
-            const bool masked = block_causal ? __any_sync(0xffffffffu, partial) : partial;
-            float* mx_tile = mx_s + (j & 1) * 256;
-            if (ok) {
-                tc_fence_after();
-                {
-                    uint32_t r[64];
-                    tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
-                }
-                // Keys past the end of the prefix or image segment do not exist.
-                if (masked) {
-                    // An opaque statement keeps this block behind its branch: the
-                    // compiler would otherwise turn it into selects run on every tile.
-                    asm volatile("");
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = visible(c) ? s[c] : -INFINITY;
-                }
-                // Partial row maximum of the raw logits (three-input max tree).
-                float t1[22];
-#pragma unroll
-                for (int i = 0; i < 21; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-                t1[21] = s[63];
-                float t2[8];
-#pragma unroll
-                for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
-                t2[7] = t1[21];
-                pmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
-                mx_tile[half * 128 + row] = pmax;
-            }
-            // The other half's maximum comes through shared memory; both warps
-            // of the pair leave this barrier with the same outcome.
-            // Both halves have read all of S_j into registers once they pass this
-            // barrier, so either may then overwrite it with its part of P_j.
-            tc_fence_before();
-            ok = named_barrier_and(pair_bar, 64, ok);
-            failed = !ok;
-            if (failed) continue;
             tc_fence_after();
-            const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
-
-            const float m_new = fmaxf(m_used, mraw * p.scale_log2);
-            const bool need = m_new > m_used + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-                if (need) m_used = m_new;
-                l_part *= alpha;
+            // Block-causal image tiles have their hidden keys written into S first
+            // (out of line); prefix keys precede every query.
+            if (kBlockCausal && j >= n_pre)   // warp-uniform
+                bc_mask_s_cold16(lane16 + scol, t_seq, reinterpret_cast<const int4*>(smem + kSmTileT), j, n_pre, L, it,
+                                 tile_valid, n_a, n_b, jq);
+            float s[64];
+            {
+                uint32_t r[64];
+                tmem_ld16x256b_x16(lane16 + scol, r);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+            }
+            // Keys past the end of the prefix or image segment do not exist:
+            // warp-uniform, so the per-element mask is a branch that full tiles
+            // skip (the opaque statement keeps the compiler from turning it into
+            // selects run on every tile).
+            if (tile_valid < kBlockN) {
+                asm volatile("");
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        s[4 * k + e] = 8 * k + 2 * jq + (e & 1) < tile_valid ? s[4 * k + e] : -INFINITY;
+            }
+            // Row maxima of the raw logits: this thread's 32 columns of each row,
+            // then the row's four threads.
+            float xa, xb;
+            {
+                float va[32], vb[32];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    va[2 * k] = s[4 * k];
+                    va[2 * k + 1] = s[4 * k + 1];
+                    vb[2 * k] = s[4 * k + 2];
+                    vb[2 * k + 1] = s[4 * k + 3];
+                }
+                xa = max32(va);
+                xb = max32(vb);
+            }
+            xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+            xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
+            xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+            xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
+            const float na = fmaxf(m_a, xa * p.scale_log2);
+            const float nb = fmaxf(m_b, xb * p.scale_log2);
+            const bool need_a = na > m_a + kRescaleThreshold;
+            const bool need_b = nb > m_b + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need_a || need_b)) {
+                const float alpha_a = need_a ? ex2(m_a - na) : 1.0f;
+                const float alpha_b = need_b ? ex2(m_b - nb) : 1.0f;
+                if (need_a) m_a = na;
+                if (need_b) m_b = nb;
+                l_a *= alpha_a;
+                l_b *= alpha_b;
                 if (j > 0) {
-                    failed = !__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (j - 1) % kSBufs),
-                                                           (uint32_t)((j - 1) / kSBufs) & 1u));
-                    if (failed) continue;
+                    if (!__all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + (j - 1) % kSBufs),
+                                                      (uint32_t)((j - 1) / kSBufs) & 1u))) {
+                        failed = true;
+                        continue;
+                    }
                     tc_fence_after();
                     uint32_t r[32];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const uint32_t ocol = lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u;
-                        tmem_ld32(ocol, r);
+                        const uint32_t ocol = lane16 + kTmO + (uint32_t)c * 64u;
+                        tmem_ld16x256b_x8(ocol, r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(ocol, r);
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) * ((i & 2) ? alpha_b : alpha_a));
+                        tmem_st16x256b_x8(ocol, r);
                     }
                     tmem_st_wait();
                 }
             }
-            // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU,
-            // four independent pair accumulators for the row sum. A hidden key's
-            // logit is -inf and stays -inf here (the scale is > 0 and m finite
-            // from the first tile on), so its p is 0.
+            // p = 2^(s*scale*log2e - m): one packed FMA per pair, ex2 on the SFU.
+            // A hidden key's logit is -inf and stays -inf here (the scale is > 0
+            // and m finite from the first tile on), so its p is 0. P_j goes over
+            // the rows' own S columns [0, 64) in the 16x128b layout: register 2k
+            // (row a) and 2k + 1 (row b) hold keys 8k + 2jq, 8k + 2jq + 1.
             const float2 cc = make_float2(p.scale_log2, p.scale_log2);
-            const float2 nm = make_float2(-m_used, -m_used);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
+            const float2 nma = make_float2(-m_a, -m_a);
+            const float2 nmb = make_float2(-m_b, -m_b);
+            float2 acc_a[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 acc_b[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
-                const float2 e = make_float2(ex2(a.x), ex2(a.y));
-                acc[c & 3] = fadd2(acc[c & 3], e);
-                pk[c] = pack_bf16x2(e.x, e.y);
+            for (int k = 0; k < 16; ++k) {
+                const float2 aa = ffma2(make_float2(s[4 * k], s[4 * k + 1]), cc, nma);
+                const float2 ab = ffma2(make_float2(s[4 * k + 2], s[4 * k + 3]), cc, nmb);
+                const float2 ea = make_float2(ex2(aa.x), ex2(aa.y));
+                const float2 eb = make_float2(ex2(ab.x), ex2(ab.y));
+                acc_a[k & 1] = fadd2(acc_a[k & 1], ea);
+                acc_b[k & 1] = fadd2(acc_b[k & 1], eb);
+                pk[2 * k] = pack_bf16x2(ea.x, ea.y);
+                pk[2 * k + 1] = pack_bf16x2(eb.x, eb.y);
             }
-            l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-            tmem_st32(lane_base + scol + (uint32_t)half * 32u, pk);
+            l_a += (acc_a[0].x + acc_a[0].y) + (acc_a[1].x + acc_a[1].y);
+            l_b += (acc_b[0].x + acc_b[0].y) + (acc_b[1].x + acc_b[1].y);
+            tmem_st16x128b_x16(lane16 + scol, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_addr(sb, BAR_P_FULL + sbuf));
@@ -758,11 +824,22 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             ok = __all_sync(0xffffffffu, wait(bar_addr(sb, BAR_PV_DONE + jl % kSBufs), (uint32_t)(jl / kSBufs) & 1u));
         }
         if (!ok) *epi_skip = 1;
-        ls_s[half * 128 + row] = l_part;
+        // Each row's sum over its four threads; the row's owner publishes it with
+        // the row's maximum.
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+        if (jq == 0) {
+            ls_s[row_a] = l_a;
+            ls_s[row_a + 8] = l_b;
+            mx_s[row_a] = m_a;
+            mx_s[row_a + 8] = m_b;
+        }
         named_barrier_sync(1, kSoftmaxThreads);
         if (!*epi_skip) {
             tc_fence_after();
-            const float l_sum = ls_s[row] + ls_s[128 + row];
+            const float l_sum = ls_s[row];
             const float inv_l = 1.0f / l_sum;
             uint8_t* stage = smem + kSmQ + (uint32_t)half * kHalfTile;   // Q is no longer read
 #pragma unroll
@@ -791,7 +868,7 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const int n = n0 + row / p.G;
             if (half == 0 && p.lse != nullptr && n < p.N) {
                 const int h = kvh * p.G + row % p.G;
-                p.lse[((int64_t)b * p.Hq + h) * p.N + n] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
+                p.lse[((int64_t)b * p.Hq + h) * p.N + n] = (mx_s[row] + log2f(l_sum)) * 0.69314718055994531f;
             }
         }
     }
@@ -1068,50 +1145,7 @@ __device__ __noinline__ int bc_next_cold(const int4* tile_t, Unit u, int t, int 
     return bc_next(tile_t, u, t, n_img);
 }
 
-// kBC, off the tile loop's hot path: the per-row mask of one 64-key half of
-// key tile j outside the unit's run, written into S in TMEM (hidden keys
-// become -inf) before the softmax loads it; called by a whole warp. Key j of
-// [prefix ; image] is visible to query i iff T_j == T_i or j <= i
-// ("Block-causal attention"). This row's 64 keys: all at or before the row or
-// all sharing its index -> nothing to hide beyond the segment end, which the
-// softmax masks itself; the row's index outside the keys' range -> causal, a
-// threshold; otherwise (a block boundary) key by key. The row is image token
-// n_row of the sequence (i = L + n_row).
-__device__ __noinline__ void bc_mask_s_cold(uint32_t taddr, const int32_t* t_img, const int4* tile_t, int j, int n_pre,
-                                            int L, int it, int half, int valid, int n_row) {
-    const int i_row = L + n_row;
-    const int t_row = __ldg(t_img + n_row);
-    const int key0 = (j < n_pre ? j * kBlockN : L + it * kBlockN) + half * 64;
-    uint64_t keep = valid >= 64 ? ~0ull : (valid <= 0 ? 0ull : (1ull << valid) - 1ull);
-    if (j >= n_pre && key0 + 63 > i_row) {
-        const int4 tr = tile_t[it];
-        const int klo = half ? tr.z : tr.x, khi = half ? tr.w : tr.y;
-        if (!(klo == t_row && khi == t_row)) {
-            const int lim = i_row - key0 + 1;   // columns c < lim are at or before the row
-            const uint64_t causal = lim >= 64 ? ~0ull : (lim <= 0 ? 0ull : (1ull << lim) - 1ull);
-            if (t_row < klo || t_row > khi) {
-                keep &= causal;
-            } else {
-                const int32_t* tk = t_img + (key0 - L);
-                for (int c = max(lim, 0); c < min(valid, 64); ++c)
-                    if (__ldg(tk + c) != t_row) keep &= ~(1ull << c);
-            }
-        }
-    }
-    if (!__any_sync(0xffffffffu, keep != ~0ull)) return;
-    __syncwarp();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t r[32];
-        tmem_ld32(taddr + 32u * (uint32_t)h, r);
-        const uint32_t kw = (uint32_t)(keep >> (32 * h));
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-            if (!((kw >> c) & 1u)) r[c] = __float_as_uint(-INFINITY);
-        tmem_st32(taddr + 32u * (uint32_t)h, r);
-    }
-    tmem_st_wait();
-}
+
 
 }  // namespace pk
 
@@ -1441,38 +1475,60 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     } else if (warp < 12) {
         // ------------------------------------------------------------ softmax + epilogue
         if constexpr (kQN) setmaxnreg_to<pk::kRegsSoftmaxQN, pk::kRegsLaunchQN>();
-        const int half = (warp - 4) >> 2;          // key columns [64*half, 64*half + 64)
+        // Warps w and w + 4 share the TMEM lanes of quadrant w & 3 and each owns
+        // 16 of its rows, read and written with the 16-lane shapes: thread
+        // 4i + jq holds rows i and i + 8 of the 16, key columns 8k + 2jq and
+        // 8k + 2jq + 1 of every group of eight. A row's maximum and sum stay
+        // within one warp (four threads), so the two warps do not meet per tile.
+        const int hw = (warp - 4) >> 2;
         const int quad = warp & 3;
+        const int jq = lane & 3;
+        const int row_a = quad * 32 + hw * 16 + (lane >> 2);   // and row_a + 8
+        const uint32_t lane16 = tmem + ((uint32_t)(quad * 32 + hw * 16) << 16);
+        // The epilogue reads O one row a thread (all 32 rows of the quadrant),
+        // 64 of its columns a warp.
         const int row = quad * 32 + lane;
         const uint32_t pair_bar = 2u + (uint32_t)quad;   // the two warps sharing these TMEM lanes
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        float* mx_s = reinterpret_cast<float*>(smem + pk::kSmMax);
-        float* ls_s = reinterpret_cast<float*>(smem + pk::kSmLsum);
+        float* rs_s = reinterpret_cast<float*>(smem + pk::kSmMax);   // [unit parity][sum, max][128 rows]
+        const int4* tile_t = reinterpret_cast<const int4*>(smem + pk::kSmTileTP);
         bool failed = false;
         int gt = 0, uq = 0;
-        // The epilogue of a unit. Both warps of a row pair reach it after the
-        // unit's tiles, failed or not, so that they meet at its pair barrier.
+        // The epilogue of a unit. Both warps of a quadrant reach it after the
+        // unit's tiles, failed or not, so that they meet at its barrier.
         struct Pending {
             int b, kvh, n0, buf, last_gt;
-            float m_used, l_part;
+            float m_a, m_b, l_a, l_b;
         };
         auto epilogue = [&](const Pending& e) {
-            // The row's two partial sums. The partner has read this slot's previous
-            // value: at least one pair barrier lies between.
-            ls_s[half * 128 + row] = e.l_part;
+            // Each row's sum over its four threads; the row's owner publishes it with
+            // the row's maximum. This parity's slot was last read two units ago,
+            // before the barrier of the unit in between.
+            float la = e.l_a, lb = e.l_b;
+            la += __shfl_xor_sync(0xffffffffu, la, 1);
+            lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+            la += __shfl_xor_sync(0xffffffffu, la, 2);
+            lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+            float* slot = rs_s + e.buf * 256;
+            if (jq == 0) {
+                slot[row_a] = la;
+                slot[row_a + 8] = lb;
+                slot[128 + row_a] = e.m_a;
+                slot[128 + row_a + 8] = e.m_b;
+            }
             if (!named_barrier_and(pair_bar, 64, !failed)) {
                 failed = true;
                 return;
             }
-            const float l_sum = ls_s[row] + ls_s[128 + row];
+            const float l_sum = slot[row];
             const int n = e.n0 + row / p.G;
-            if (half == 0 && p.lse != nullptr && n < p.N) {
+            if (hw == 0 && p.lse != nullptr && n < p.N) {
                 const int h = e.kvh * p.G + row % p.G;
-                p.lse[((int64_t)e.b * p.Hq + h) * p.N + n] = (e.m_used + log2f(l_sum)) * 0.69314718055994531f;
+                p.lse[((int64_t)e.b * p.Hq + h) * p.N + n] = (slot[128 + row] + log2f(l_sum)) * 0.69314718055994531f;
             }
             // A warp whose wait fails skips the arrivals below; the roles waiting on
             // them then see the abort flag, and its partner learns of the failure at
-            // the next pair barrier.
+            // the next epilogue barrier.
             if (!__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + e.last_gt % kSBufs),
                                               (uint32_t)(e.last_gt / kSBufs) & 1u))) {
                 failed = true;
@@ -1482,12 +1538,12 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             const float inv_l = 1.0f / l_sum;
             uint32_t r[2][32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u, r[c]);
+            for (int c = 0; c < 2; ++c) tmem_ld32(lane_base + kTmO + (uint32_t)hw * 64u + (uint32_t)c * 32u, r[c]);
             // O is read: the next unit's first PV may overwrite it.
             tc_fence_before();
             mbar_arrive(bar(sb, O_FREE));
             // The unit's Q buffer (its last S has completed) stages the output.
-            uint8_t* stage = smem + kSmQ0 + (uint32_t)e.buf * kTile + (uint32_t)half * kHalfTile;
+            uint8_t* stage = smem + kSmQ0 + (uint32_t)e.buf * kTile + (uint32_t)hw * kHalfTile;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -1511,117 +1567,129 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             const Unit u = nxt;
             const bool more = U + ncl < n_units;
             const UnitLoad ahead = more ? load_unit(p, U + ncl, pairs) : UnitLoad{0, 0, 0};
-            float m_used = -INFINITY;
-            float l_part = 0.f;
+            float m_a = -INFINITY, m_b = -INFINITY;   // running maxima of rows a and a + 8 (log2 units)
+            float l_a = 0.f, l_b = 0.f;               // this thread's part of their sums
             if (u.n_tiles > 0) {
-                // kBC: this row's query is image token n_row (clamped for padding
-                // rows, whose output is never stored), L + n_row in the
-                // concatenated order [prefix ; image].
-                const int n_row = min(u.n0 + row / p.G, p.N - 1);
+                // kBC: the rows' queries are image tokens n_a, n_b (clamped for
+                // padding rows, whose output is never stored).
+                const int n_a = min(u.n0 + row_a / p.G, p.N - 1);
+                const int n_b = min(u.n0 + (row_a + 8) / p.G, p.N - 1);
                 int it = -1;                       // image tile of key tile j
-                // A failed wait sets `failed`: the loops then keep running without
-                // touching TMEM or the pipeline barriers, so that the two warps of a
-                // row pair still meet at every pair barrier.
+                // A failed wait sets `failed`: the loop then runs on without touching
+                // TMEM or the pipeline barriers, to the unit's epilogue barrier.
                 for (int j = 0; j < u.n_tiles; ++j, ++gt) {
                     // Image tiles up to the diagonal and those of the run follow one
                     // another; only kept tiles past both are looked up.
                     if (j >= u.n_pre)
                         it = kBC && j >= u.run && j - u.n_pre > u.j_diag
-                                 ? pk::bc_next_cold(reinterpret_cast<const int4*>(smem + pk::kSmTileTP), u, it, n_img)
+                                 ? pk::bc_next_cold(tile_t, u, it, n_img)
                                  : j - u.n_pre;
+                    if (failed) continue;
                     const int sbuf = gt % kSBufs;
                     const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
-                    bool ok = !failed && __all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u));
-                    float s[64];
-                    float pmax = -INFINITY;
-                    const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
-                    const int valid = tile_valid - half * 64;    // may be <= 0: this half is all padding
-                    // Keys past the end of the prefix or image segment do not exist:
-                    // warp-uniform, so the per-element mask below is a branch that
-                    // full tiles skip. A block-causal tile outside the unit's run also
-                    // has its hidden keys written into S first (out of line).
-                    const bool partial = valid < 64;
-                    float* mx_tile = mx_s + (gt & 1) * 256;
-                    if (ok) {
-                        tc_fence_after();
-                        if (kBC && j >= u.run)   // warp-uniform
-                            pk::bc_mask_s_cold(lane_base + scol + (uint32_t)half * 64u, p.t_img,
-                                               reinterpret_cast<const int4*>(smem + pk::kSmTileTP), j, u.n_pre, u.L,
-                                               it, half, valid, n_row);
-                        {
-                            uint32_t r[64];
-                            tmem_ld64(lane_base + scol + (uint32_t)half * 64u, r);
-    #pragma unroll
-                            for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
-                        }
-                        if (partial) {
-                            // An opaque statement keeps this block behind its branch: the
-                            // compiler would otherwise turn it into selects run on every tile.
-                            asm volatile("");
-    #pragma unroll
-                            for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
-                        }
-                        // Partial row maximum of the raw logits (three-input max tree).
-                        float t1[22];
-    #pragma unroll
-                        for (int i = 0; i < 21; ++i) t1[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-                        t1[21] = s[63];
-                        float t2[8];
-    #pragma unroll
-                        for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
-                        t2[7] = t1[21];
-                        pmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
-                        mx_tile[half * 128 + row] = pmax;
+                    if (!__all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u))) {
+                        failed = true;
+                        continue;
                     }
-                    // The other half's maximum comes through shared memory; both warps of
-                    // the pair leave this barrier with the same outcome, and both have read
-                    // all of S into registers, so either may then overwrite it with P.
-                    tc_fence_before();
-                    ok = named_barrier_and(pair_bar, 64, ok);
-                    failed = !ok;
-                    if (failed) continue;
+                    const int tile_valid = j < u.n_pre ? min(kBlockN, u.L - j * kBlockN) : min(kBlockN, p.N - it * kBlockN);
                     tc_fence_after();
-                    const float mraw = fmaxf(pmax, mx_tile[(half ^ 1) * 128 + row]);
-                    const float m_new = fmaxf(m_used, mraw * p.scale_log2);
-                    const bool need = m_new > m_used + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-                        if (need) m_used = m_new;
-                        l_part *= alpha;
+                    // A block-causal tile outside the unit's run has its hidden keys
+                    // written into S first (out of line).
+                    if (kBC && j >= u.run)   // warp-uniform
+                        bc_mask_s_cold16(lane16 + scol, p.t_img, tile_t, j, u.n_pre, u.L, it, tile_valid, n_a, n_b, jq);
+                    float s[64];
+                    {
+                        uint32_t r[64];
+                        tmem_ld16x256b_x16(lane16 + scol, r);
+    #pragma unroll
+                        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+                    }
+                    // Keys past the end of the prefix or image segment do not exist:
+                    // warp-uniform, so the per-element mask is a branch that full tiles
+                    // skip (the opaque statement keeps the compiler from turning it
+                    // into selects run on every tile).
+                    if (tile_valid < kBlockN) {
+                        asm volatile("");
+    #pragma unroll
+                        for (int k = 0; k < 16; ++k)
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                s[4 * k + e] = 8 * k + 2 * jq + (e & 1) < tile_valid ? s[4 * k + e] : -INFINITY;
+                    }
+                    // Row maxima of the raw logits: this thread's 32 columns of each row
+                    // (three-input max trees), then the row's four threads.
+                    float xa, xb;
+                    {
+                        float va[32], vb[32];
+    #pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            va[2 * k] = s[4 * k];
+                            va[2 * k + 1] = s[4 * k + 1];
+                            vb[2 * k] = s[4 * k + 2];
+                            vb[2 * k + 1] = s[4 * k + 3];
+                        }
+                        xa = max32(va);
+                        xb = max32(vb);
+                    }
+                    xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+                    xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
+                    xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+                    xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
+                    const float na = fmaxf(m_a, xa * p.scale_log2);
+                    const float nb = fmaxf(m_b, xb * p.scale_log2);
+                    const bool need_a = na > m_a + kRescaleThreshold;
+                    const bool need_b = nb > m_b + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, need_a || need_b)) {
+                        const float alpha_a = need_a ? ex2(m_a - na) : 1.0f;
+                        const float alpha_b = need_b ? ex2(m_b - nb) : 1.0f;
+                        if (need_a) m_a = na;
+                        if (need_b) m_b = nb;
+                        l_a *= alpha_a;
+                        l_b *= alpha_b;
                         if (j > 0) {
-                            failed = !__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + (gt - 1) % kSBufs),
-                                                                   (uint32_t)((gt - 1) / kSBufs) & 1u));
-                            if (failed) continue;
+                            if (!__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + (gt - 1) % kSBufs),
+                                                              (uint32_t)((gt - 1) / kSBufs) & 1u))) {
+                                failed = true;
+                                continue;
+                            }
                             tc_fence_after();
                             uint32_t r[32];
     #pragma unroll
                             for (int c = 0; c < 2; ++c) {
-                                const uint32_t ocol = lane_base + kTmO + (uint32_t)half * 64u + (uint32_t)c * 32u;
-                                tmem_ld32(ocol, r);
+                                const uint32_t ocol = lane16 + kTmO + (uint32_t)c * 64u;
+                                tmem_ld16x256b_x8(ocol, r);
     #pragma unroll
-                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                                tmem_st32(ocol, r);
+                                for (int i = 0; i < 32; ++i)
+                                    r[i] = __float_as_uint(__uint_as_float(r[i]) * ((i & 2) ? alpha_b : alpha_a));
+                                tmem_st16x256b_x8(ocol, r);
                             }
                             tmem_st_wait();
                         }
                     }
                     // p = 2^(s*scale*log2e - m): a hidden key's -inf logit stays -inf
                     // (the scale is > 0 and m finite from the first tile on), so its p is 0.
+                    // P_j goes over the rows' own S columns [0, 64) in the 16x128b layout:
+                    // register 2k (row a) and 2k + 1 (row b) hold keys 8k + 2jq, 8k + 2jq + 1.
                     const float2 cc = make_float2(p.scale_log2, p.scale_log2);
-                    const float2 nm = make_float2(-m_used, -m_used);
-                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                     make_float2(0.f, 0.f)};
+                    const float2 nma = make_float2(-m_a, -m_a);
+                    const float2 nmb = make_float2(-m_b, -m_b);
+                    float2 acc_a[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    float2 acc_b[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     uint32_t pk[32];
     #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float2 a = ffma2(make_float2(s[2 * c], s[2 * c + 1]), cc, nm);
-                        const float2 e = make_float2(ex2(a.x), ex2(a.y));
-                        acc[c & 3] = fadd2(acc[c & 3], e);
-                        pk[c] = pack_bf16x2(e.x, e.y);
+                    for (int k = 0; k < 16; ++k) {
+                        const float2 aa = ffma2(make_float2(s[4 * k], s[4 * k + 1]), cc, nma);
+                        const float2 ab = ffma2(make_float2(s[4 * k + 2], s[4 * k + 3]), cc, nmb);
+                        const float2 ea = make_float2(ex2(aa.x), ex2(aa.y));
+                        const float2 eb = make_float2(ex2(ab.x), ex2(ab.y));
+                        acc_a[k & 1] = fadd2(acc_a[k & 1], ea);
+                        acc_b[k & 1] = fadd2(acc_b[k & 1], eb);
+                        pk[2 * k] = pack_bf16x2(ea.x, ea.y);
+                        pk[2 * k + 1] = pack_bf16x2(eb.x, eb.y);
                     }
-                    l_part += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                              ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-                    tmem_st32(lane_base + scol + (uint32_t)half * 32u, pk);
+                    l_a += (acc_a[0].x + acc_a[0].y) + (acc_a[1].x + acc_a[1].y);
+                    l_b += (acc_b[0].x + acc_b[0].y) + (acc_b[1].x + acc_b[1].y);
+                    tmem_st16x128b_x16(lane16 + scol, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(bar(sb, P_FULL + sbuf));
@@ -1630,7 +1698,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             // Before the epilogue, whose wait for the last PV hides it.
             if (more) nxt = finish_unit<kBC>(p, ahead, pairs, crank, smem);
             if (u.n_tiles > 0) {
-                epilogue(Pending{u.b, u.kvh, u.n0, uq & 1, gt - 1, m_used, l_part});
+                epilogue(Pending{u.b, u.kvh, u.n0, uq & 1, gt - 1, m_a, m_b, l_a, l_b});
                 ++uq;
             }
         }

@@ -90,9 +90,9 @@ constexpr uint32_t kTile = 2u * kHalfTile;         // 128 rows x 128 bf16
 constexpr uint32_t kSmQ = 0;
 constexpr uint32_t kSmK = kSmQ + kTile;
 constexpr uint32_t kSmV = kSmK + kKStages * kTile;
-constexpr uint32_t kSmMax = kSmV + kVStages * kTile;   // float [2 tile parity][2 halves][128 rows]
-constexpr uint32_t kSmLsum = kSmMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]
-constexpr uint32_t kSmBar = kSmLsum + 2 * 128 * 4;
+constexpr uint32_t kSmMax = kSmV + kVStages * kTile;   // float [128 rows]: the rows' running maxima
+constexpr uint32_t kSmLsum = kSmMax + 128 * 4;         // float [128 rows]: the rows' sums
+constexpr uint32_t kSmBar = kSmLsum + 128 * 4;
 
 enum : int {
     BAR_Q_FULL = 0,
@@ -948,9 +948,8 @@ static_assert(128 * kRegsRolesQN + 256 * kRegsSoftmaxQN + 128 * kRegsNormQN <= k
 constexpr uint32_t kSmQ0 = 0;                      // Q buffers 0 and 1 (also output staging)
 constexpr uint32_t kSmK = 2 * kTile;
 constexpr uint32_t kSmV = kSmK + kKStages * kTile;
-constexpr uint32_t kSmMax = kSmV + kVStages * kTile;   // float [2 tile parity][2 halves][128 rows]
-constexpr uint32_t kSmLsum = kSmMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]
-constexpr uint32_t kSmTileTP = kSmLsum + 2 * 128 * 4;  // int4 [kMaxImgTiles] (kBC): min0 max0 min1 max1
+constexpr uint32_t kSmRowStats = kSmV + kVStages * kTile;   // float [2 unit parity][sum, max][128 rows]
+constexpr uint32_t kSmTileTP = kSmRowStats + 2 * 2 * 128 * 4;  // int4 [kMaxImgTiles] (kBC): min0 max0 min1 max1
 constexpr int kMaxUnitsBC = 2048;                      // kBC: units a cluster may take (host-checked)
 constexpr uint32_t kSmUnitTiles = kSmTileTP + kMaxImgTiles * 16;   // int [kMaxUnitsBC] (kBC): key tiles of unit k
 constexpr uint32_t kSmQnWP = kSmUnitTiles + kMaxUnitsBC * 4;   // float [128] (kQN): the q norm weights
@@ -1490,7 +1489,7 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         const int row = quad * 32 + lane;
         const uint32_t pair_bar = 2u + (uint32_t)quad;   // the two warps sharing these TMEM lanes
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        float* rs_s = reinterpret_cast<float*>(smem + pk::kSmMax);   // [unit parity][sum, max][128 rows]
+        float* rs_s = reinterpret_cast<float*>(smem + pk::kSmRowStats);   // [unit parity][sum, max][128 rows]
         const int4* tile_t = reinterpret_cast<const int4*>(smem + pk::kSmTileTP);
         bool failed = false;
         int gt = 0, uq = 0;

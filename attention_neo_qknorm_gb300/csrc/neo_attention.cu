@@ -896,8 +896,10 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 //   * Q is double-buffered. The next unit's Q is loaded kQLead tiles before
 //     the current unit's last K tile; a unit's Q buffer becomes the staging
 //     buffer of its output once its last S has completed.
-//   * The softmax threads' part of the epilogue is short: the row pair's
-//     partial sums are combined (one pair barrier), the LSE is written, then
+//   * The softmax threads' part of the epilogue is short: each row's sum is
+//     combined over its four threads and published with the row's maximum in
+//     shared memory (one barrier of the two warps of a sub-partition, the
+//     only point where they meet), the LSE is written, then
 //     O is read from TMEM (O_FREE: the next unit's first PV may overwrite it),
 //     normalised and staged; each thread then arrives on STAGED and goes on
 //     to the next unit. The Q/K producer lane issues the staged tile's TMA
@@ -909,8 +911,8 @@ gen_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 //   * The S issuer holds a unit's second S until the previous unit's last PV
 //     has completed, so that PV, which the epilogue waits for, is not queued
 //     behind two S batches of the next unit.
-//   * K and V rings, S buffers and the pair exchange run on one tile counter
-//     across units. K has two stages here to make room for the second Q.
+//   * K and V rings and S buffers run on one tile counter across units. K has
+//     two stages here to make room for the second Q.
 // The softmax of a tile is the same as in gen_attention_kernel.
 //
 // Block-causal instantiation (kBC, one sequence: a prefill): the temporal-
@@ -939,7 +941,7 @@ constexpr int kQLead = 4;                          // tiles ahead that the next 
 constexpr int kQLeadQN = 12;                       // ... with the folded query norm
 constexpr int kThreadsQN = 512;                    // kQN: 16 warps
 constexpr int kQnWarp0 = 12;                       // kQN: the norm warpgroup, warps 12..15
-constexpr uint32_t kQnBar = 6;                     // its named barrier (2..5 are the row pairs')
+constexpr uint32_t kQnBar = 6;                     // its named barrier (2..5: the sub-partitions' epilogues)
 constexpr int kRegsLaunchQN = 65536 / kThreadsQN;      // registers a thread at launch (__launch_bounds__)
 constexpr int kRegsRolesQN = 72, kRegsSoftmaxQN = 168, kRegsNormQN = 104;
 static_assert(128 * kRegsRolesQN + 256 * kRegsSoftmaxQN + 128 * kRegsNormQN <= kThreadsQN * kRegsLaunchQN,

@@ -1495,6 +1495,8 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         const int4* tile_t = reinterpret_cast<const int4*>(smem + pk::kSmTileTP);
         bool failed = false;
         int gt = 0, uq = 0;
+        int sbuf = 0;                              // gt % kSBufs
+        uint32_t sphase = 0;                       // (gt / kSBufs) & 1
         // The epilogue of a unit. Both warps of a quadrant reach it after the
         // unit's tiles, failed or not, so that they meet at its barrier.
         struct Pending {
@@ -1578,7 +1580,8 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 int it = -1;                       // image tile of key tile j
                 // A failed wait sets `failed`: the loop then runs on without touching
                 // TMEM or the pipeline barriers, to the unit's epilogue barrier.
-                for (int j = 0; j < u.n_tiles; ++j, ++gt) {
+                for (int j = 0; j < u.n_tiles;
+                     ++j, ++gt, sphase ^= (sbuf == kSBufs - 1) ? 1u : 0u, sbuf = sbuf == kSBufs - 1 ? 0 : sbuf + 1) {
                     // Image tiles up to the diagonal and those of the run follow one
                     // another; only kept tiles past both are looked up.
                     if (j >= u.n_pre)
@@ -1586,9 +1589,8 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                                  ? pk::bc_next_cold(tile_t, u, it, n_img)
                                  : j - u.n_pre;
                     if (failed) continue;
-                    const int sbuf = gt % kSBufs;
                     const uint32_t scol = kTmS0 + (uint32_t)sbuf * 128u;
-                    if (!__all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), (uint32_t)(gt / kSBufs) & 1u))) {
+                    if (!__all_sync(0xffffffffu, wait(bar(sb, S_FULL + sbuf), sphase))) {
                         failed = true;
                         continue;
                     }
@@ -1648,8 +1650,8 @@ gen_attention_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                         l_a *= alpha_a;
                         l_b *= alpha_b;
                         if (j > 0) {
-                            if (!__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + (gt - 1) % kSBufs),
-                                                              (uint32_t)((gt - 1) / kSBufs) & 1u))) {
+                            const int pbuf = sbuf == 0 ? kSBufs - 1 : sbuf - 1;   // tile gt - 1
+                            if (!__all_sync(0xffffffffu, wait(bar(sb, PV_DONE + pbuf), sbuf == 0 ? sphase ^ 1u : sphase))) {
                                 failed = true;
                                 continue;
                             }

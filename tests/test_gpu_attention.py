@@ -57,6 +57,57 @@ def test_attention_large_logits(gpu_lib):
     run_case((300,), 200, 8, 2, scale=0.35, seed=6)
 
 
+def _spike_inputs(B, L, N, Hq, Hkv, seed):
+    """Small random Q/K plus one spike key per query row: row r of a 128-row
+    query tile (token n, head h: r = (n % (128 / G)) * G + h % G) has a large
+    component in dimension r, and the key 128 T_r + r of the concatenated
+    [prefix ; image] sequence, T_r = 1 + (r // 8) % 3, has one in the same
+    dimension. Each row's running maximum then jumps by ~18 (log2 units) at
+    its own key tile T_r, and rows r and r + 8 jump at different tiles."""
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(seed)
+    q = 0.1 * torch.randn(B, N, Hq, 128, generator=g)
+    kp = 0.1 * torch.randn(B * L, Hkv, 128, generator=g)
+    k = 0.1 * torch.randn(B, N, Hkv, 128, generator=g)
+    v = torch.randn(B, N, Hkv, 128, generator=g)
+    vp = torch.randn(B * L, Hkv, 128, generator=g)
+    for n in range(N):
+        for h in range(Hq):
+            q[:, n, h, (n % (128 // G)) * G + h % G] += 12.0
+    for r in range(128):
+        j = 128 * (1 + (r // 8) % 3) + r
+        for b in range(B):
+            if j < L:
+                kp[b * L + j, :, r] += 12.0
+            elif j - L < N:
+                k[b, j - L, :, r] += 12.0
+    bf = lambda t: t.to(torch.bfloat16)
+    return bf(q), bf(kp), bf(vp), bf(k), bf(v)
+
+
+@pytest.mark.parametrize("block_causal", [False, True])
+def test_attention_rows_of_one_thread_rescale_at_different_tiles(gpu_lib, block_causal):
+    """The output rescale of one row on a tile where its thread's other row
+    (eight lanes further) keeps its maximum, in the persistent kernel (full
+    mask, one sequence) and in the one-tile kernel (two block-causal
+    sequences whose generation positions make the mask full)."""
+    B, L, N, Hq, Hkv = (2 if block_causal else 1), 200, 300, 8, 2
+    q, kp, vp, k, v = _spike_inputs(B, L, N, Hq, Hkv, seed=21)
+    cu = np.arange(B + 1, dtype=np.int32) * L
+    out = torch.full((B, N, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq, N), float("nan"), device="cuda")
+    kw = {}
+    if block_causal:
+        kw = dict(mask_mode=neo.NEO_MASK_BLOCK_CAUSAL,
+                  t_prefix=torch.arange(L, dtype=torch.int32).repeat(B).cuda(),
+                  t_img=torch.full((B * N,), L, dtype=torch.int32).cuda())
+    neo.neo_gen_attention(q.cuda(), kp.cuda(), vp.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cu).cuda(), L, out,
+                          scale=SCALE, lse=lse, **kw)
+    ref, ref_lse = O.gen_attention(f64(q), f64(kp), f64(vp), f64(k), f64(v), cu, SCALE)
+    assert_bf16_close(f64(out), ref, f"spike keys, block_causal={block_causal}")
+    np.testing.assert_allclose(f64(lse), ref_lse, rtol=1e-4, atol=1e-3)
+
+
 def test_attention_without_lse_and_repeated_calls(gpu_lib):
     a = run_case((150,), 140, 8, 2, seed=8, lse=False)
     b = run_case((150,), 140, 8, 2, seed=8, lse=False)

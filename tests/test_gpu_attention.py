@@ -108,6 +108,46 @@ def test_attention_rows_of_one_thread_rescale_at_different_tiles(gpu_lib, block_
     np.testing.assert_allclose(f64(lse), ref_lse, rtol=1e-4, atol=1e-3)
 
 
+def _random_shape(rng):
+    Hkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.integers(1, 4))
+    prefix = tuple(int(x) for x in rng.integers(0, 300, size=B))
+    N = int(rng.integers(1, 300))
+    return prefix, N, G * Hkv, Hkv
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_attention_random_shapes(gpu_lib, case):
+    """Seeded random prefix lengths, image lengths, group sizes and sequence
+    counts: partial key tiles of every width and query tiles cut anywhere
+    within a softmax warp's 16 rows."""
+    rng = np.random.default_rng(1000 + case)
+    prefix, N, Hq, Hkv = _random_shape(rng)
+    run_case(prefix, N, Hq, Hkv, seed=case, lse=bool(case % 2))
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_block_causal_random_shapes(gpu_lib, case):
+    """The block-causal mask on seeded random shapes and temporal indexes (a
+    text run, an image block sharing one index, more text; the query segment
+    cut at a random point), one sequence (persistent kernel) or two (one query
+    tile per CTA)."""
+    rng = np.random.default_rng(2000 + case)
+    B = 1 + case % 2
+    Hkv = int(rng.choice([1, 2]))
+    Hq = Hkv * int(rng.choice([1, 4]))
+    pre, img = [], []
+    for _ in range(B):
+        t = _mixed_T(int(rng.integers(1, 120)), int(rng.integers(1, 200)), int(rng.integers(1, 120)))
+        cut = int(rng.integers(0, len(t) // 2))
+        pre.append(t[:cut])
+        img.append(t[cut:])
+    n = min(len(x) for x in img)
+    img = [x[:n] for x in img]
+    _block_causal_case(pre, img, Hq=Hq, Hkv=Hkv, seed=case)
+
+
 def test_attention_without_lse_and_repeated_calls(gpu_lib):
     a = run_case((150,), 140, 8, 2, seed=8, lse=False)
     b = run_case((150,), 140, 8, 2, seed=8, lse=False)

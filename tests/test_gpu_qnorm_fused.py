@@ -39,6 +39,26 @@ def test_fused_equals_two_launches(gpu_lib, prefix, grid, Hq, Hkv):
     assert torch.equal(a.lse, b.lse)
 
 
+@pytest.mark.parametrize("case", range(8))
+def test_fused_equals_two_launches_random_shapes(gpu_lib, case):
+    """Seeded random prefixes, grids and group sizes."""
+    rng = np.random.default_rng(3000 + case)
+    Hkv = int(rng.choice([1, 2]))
+    Hq = Hkv * int(rng.choice([1, 2, 4, 8]))
+    prefix = tuple(int(x) for x in rng.integers(0, 300, size=int(rng.integers(1, 4))))
+    grid = (int(rng.integers(1, 18)), int(rng.integers(1, 18)))
+    w = synth.small_workload(prefix=prefix, grid=grid, Hq=Hq, Hkv=Hkv, B=len(prefix))
+    inp = synth.make_inputs(w, seed=50 + case)
+    a = GpuLayer(w, inp)
+    b = GpuLayer(w, inp)
+    a.norm_rope()
+    a.attention()
+    b.norm_rope_k()
+    b.attention_qnorm()
+    assert torch.equal(a.out, b.out), f"fused and two-launch outputs differ: {prefix} {grid} {Hq}/{Hkv}"
+    assert torch.equal(a.lse, b.lse)
+
+
 def test_fused_matches_oracle_with_distinct_positions(gpu_lib):
     """Positions that differ on all three axes per token (a prefix of text
     tokens as the query segment): the temporal angle is not constant."""
